@@ -1,0 +1,79 @@
+"""Plain definitions of the tile orders (pure integer arithmetic, slow and obvious).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  Shares no code with
+the CUDA scheduler; the tests compare the two mapping by mapping.
+
+A *unit* is one CTA work item: the ``bm`` query rows ``[m*bm, (m+1)*bm)`` of
+query head ``h`` in batch ``b``.  ``nb = ceil(N / bm)`` row blocks per head.
+
+Orders (the pages' names, detail page of "Optimizing Attention on GPUs by
+Exploiting GPU Architectural NUMA Effects", section 2 Q2 and section 3
+"before/after" table):
+
+* head-first: all row blocks of one Attention Compute Cluster (the query
+  heads that share one KV head) before the next one.  With contiguous GQA
+  groups, (batch, kv group, head in group, block) order is simply
+  (batch, head, block).
+* block-first: all heads of one row block before the next row block.
+* naive head-first: the head-first linear order, but each unit is its own
+  CTA and the hardware decides where it runs.
+
+For causal attention the blocks of a head are visited last-block-first, so
+the longest units start first (the pages give only "ACC before next ACC";
+this within-ACC order is a reading).
+"""
+from __future__ import annotations
+
+HEAD_FIRST = 0
+BLOCK_FIRST = 1
+NAIVE_HEAD_FIRST = 2
+ORDERS = (HEAD_FIRST, BLOCK_FIRST, NAIVE_HEAD_FIRST)
+
+
+def num_blocks(n: int, bm: int) -> int:
+    return -(-n // bm)
+
+
+def unit_to_tile(order: int, u: int, batch: int, heads: int, nb: int, causal: bool):
+    """Linear unit id -> (b, h, m)."""
+    total = batch * heads * nb
+    if not 0 <= u < total:
+        raise ValueError("unit out of range")
+    if order in (HEAD_FIRST, NAIVE_HEAD_FIRST):
+        bh, r = divmod(u, nb)
+        b, h = divmod(bh, heads)
+    elif order == BLOCK_FIRST:
+        bm_, h = divmod(u, heads)
+        b, r = divmod(bm_, nb)
+    else:
+        raise ValueError("unknown order")
+    m = nb - 1 - r if causal else r
+    return b, h, m
+
+
+def swizzled_head_first(wid: int, batch: int, heads: int, blocks_per_head: int, num_xcd: int):
+    """The pages' Swizzled Head-first WG-ID remap (detail page, section 7,
+    Figure 11 key code), returning (batch, head, block).
+
+    Reading of a garbled line: the page computes the per-batch id as
+    ``wid // BATCH`` while taking the batch as ``(wid // (blocks*H)) % BATCH``;
+    the two disagree for BATCH > 1 (the map is then not one-to-one).  Here the
+    batch is outermost and the per-batch id is ``wid % (H * blocks)``, which
+    agrees with the printed code for BATCH = 1.
+    """
+    if heads % num_xcd:
+        raise ValueError("heads must be a multiple of num_xcd (pages give no fallback)")
+    per_batch = heads * blocks_per_head
+    wid_pb = wid % per_batch
+    heads_per_xcd = heads // num_xcd
+    chunk = num_xcd * blocks_per_head
+    head = (wid_pb % num_xcd) * heads_per_xcd + wid_pb // (num_xcd * blocks_per_head)
+    block = (wid_pb % chunk) // num_xcd
+    b = (wid // per_batch) % batch
+    return b, head, block
+
+
+def swizzle_chiplet(wgid: int, grid: int, num_xcd: int) -> int:
+    """The chiplet swizzle baseline (detail page, section 7, Figure 3)."""
+    per_xcd = grid // num_xcd
+    return (wgid % num_xcd) * per_xcd + wgid // num_xcd

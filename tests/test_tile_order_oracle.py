@@ -1,0 +1,102 @@
+"""Pins for the tile-order definitions (integer, exhaustive).  CPU only."""
+import pytest
+
+from oracle import tile_order as T
+
+
+@pytest.mark.parametrize("order", T.ORDERS)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,nb", [(1, 2, 1), (1, 8, 5), (2, 3, 4), (4, 128, 3), (1, 64, 32)])
+def test_orders_are_bijections(order, causal, B, H, nb):
+    seen = {T.unit_to_tile(order, u, B, H, nb, causal) for u in range(B * H * nb)}
+    assert seen == {(b, h, m) for b in range(B) for h in range(H) for m in range(nb)}
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_first_finishes_a_head_before_the_next(causal):
+    B, H, nb = 2, 6, 7
+    seq = [T.unit_to_tile(T.HEAD_FIRST, u, B, H, nb, causal) for u in range(B * H * nb)]
+    for i in range(0, len(seq), nb):  # each run of nb units is one (b, h)
+        assert len({(b, h) for b, h, _ in seq[i:i + nb]}) == 1
+    if causal:  # longest (last) block first inside each head
+        assert [m for _, _, m in seq[:nb]] == list(range(nb - 1, -1, -1))
+
+
+def test_head_first_keeps_a_gqa_group_together():
+    """Query heads of one KV group (contiguous groups) are consecutive."""
+    B, Hq, Hkv, nb = 1, 16, 4, 3
+    G = Hq // Hkv
+    groups = [T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, False)[1] // G for u in range(B * Hq * nb)]
+    assert groups == sorted(groups)
+
+
+def test_block_first_cycles_heads_innermost():
+    B, H, nb = 1, 5, 4
+    seq = [T.unit_to_tile(T.BLOCK_FIRST, u, B, H, nb, False) for u in range(H * nb)]
+    assert [h for _, h, _ in seq[:H]] == list(range(H))
+    assert {m for _, _, m in seq[:H]} == {0}
+
+
+def test_naive_head_first_has_the_head_first_linear_order():
+    for u in range(2 * 3 * 4):
+        assert (T.unit_to_tile(T.NAIVE_HEAD_FIRST, u, 2, 3, 4, True)
+                == T.unit_to_tile(T.HEAD_FIRST, u, 2, 3, 4, True))
+
+
+@pytest.mark.parametrize("B", [1, 2, 4])
+@pytest.mark.parametrize("H", [8, 128])
+@pytest.mark.parametrize("X", [1, 4, 8])
+def test_swizzle_is_a_bijection(B, H, X):
+    nb = 16
+    seen = {T.swizzled_head_first(w, B, H, nb, X) for w in range(B * H * nb)}
+    assert len(seen) == B * H * nb
+    assert all(0 <= b < B and 0 <= h < H and 0 <= m < nb for b, h, m in seen)
+
+
+def test_swizzle_figure10_each_head_on_one_xcd():
+    """Figure 10 of the detail page: 8 query heads, 128 row blocks, 4 XCDs; with
+    round-robin dispatch (WG w runs on XCD w % 4) every head lands on one XCD."""
+    H, nb, X = 8, 128, 4
+    xcd_of_head = {}
+    for w in range(H * nb):
+        _, h, _ = T.swizzled_head_first(w, 1, H, nb, X)
+        xcd_of_head.setdefault(h, set()).add(w % X)
+    assert all(len(s) == 1 for s in xcd_of_head.values())
+    # two heads per XCD, each XCD used
+    per_xcd = {}
+    for h, s in xcd_of_head.items():
+        per_xcd.setdefault(next(iter(s)), []).append(h)
+    assert sorted(len(v) for v in per_xcd.values()) == [2, 2, 2, 2]
+
+
+def test_swizzle_with_one_xcd_is_naive_head_first():
+    B, H, nb = 2, 8, 9
+    for w in range(B * H * nb):
+        assert T.swizzled_head_first(w, B, H, nb, 1) == T.unit_to_tile(T.HEAD_FIRST, w, B, H, nb, False)
+
+
+def test_swizzle_printed_batch_line_is_not_a_bijection_for_two_batches():
+    """The page's per-batch id ``wid // BATCH`` (read literally) collides for
+    BATCH = 2; this is why the reading ``wid % (H * blocks)`` is used."""
+    B, H, nb, X = 2, 8, 4, 4
+
+    def literal(wid):
+        wpb = wid // B
+        hpx = H // X
+        head = (wpb % X) * hpx + wpb // (X * nb)
+        block = (wpb % (X * nb)) // X
+        batch = (wid // (nb * H)) % B
+        return batch, head, block
+
+    assert len({literal(w) for w in range(B * H * nb)}) < B * H * nb
+    assert len({T.swizzled_head_first(w, B, H, nb, X) for w in range(B * H * nb)}) == B * H * nb
+
+
+def test_swizzle_rejects_heads_not_divisible_by_xcds():
+    with pytest.raises(ValueError):
+        T.swizzled_head_first(0, 1, 12, 4, 8)
+
+
+def test_chiplet_swizzle_is_a_permutation():
+    for X, grid in [(8, 64), (4, 4096)]:
+        assert sorted(T.swizzle_chiplet(w, grid, X) for w in range(grid)) == list(range(grid))
