@@ -1,0 +1,182 @@
+"""Python binding of libattn.so (fused attention for GB300 / sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/attn.h``.  The functions take
+torch tensors (for device memory and the current stream) and return the
+library's status code; ``check`` turns a non-zero code into an exception.
+There is no fallback: if ``libattn.so`` cannot be loaded, importing the
+functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_WORKSPACE = -3
+ATTN_ERR_CUDA = -4
+ATTN_ERR_TIMEOUT = -5
+
+ORDER_HEAD_FIRST = 0
+ORDER_BLOCK_FIRST = 1
+ORDER_NAIVE_HEAD_FIRST = 2
+ORDERS = {"head_first": ORDER_HEAD_FIRST, "block_first": ORDER_BLOCK_FIRST,
+          "naive_head_first": ORDER_NAIVE_HEAD_FIRST}
+
+# Every symbol include/attn.h declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_LL = ctypes.c_longlong
+_SZ = ctypes.c_size_t
+_IP = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
+    "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "attn_decode_num_splits": (_I, [_I, _I, _I, _I]),
+    "attn_tile_map": (_I, [_I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
+    "attn_fwd_units": (_LL, [_I, _I, _I]),
+    "attn_device_status": (_I, [_P]),
+    "attn_set_wait_timeout_ns": (_LL, [_LL]),
+    "attn_strerror": (ctypes.c_char_p, [_I]),
+    "attn_version": (_I, []),
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})" if what else f"{strerror(code)} ({code})")
+
+
+def lib():
+    """Load libattn.so (raises OSError / RuntimeError when it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "attention_fa2_fwd_sm_gb300._build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().attn_strerror(int(code)).decode()
+
+
+def check(code: int, what: str = "") -> None:
+    if code != ATTN_OK:
+        raise AttnError(code, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, stream=None) -> int:
+    return lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+                          float(scale), int(bool(causal)), _stream(stream))
+
+
+def attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, stream=None) -> int:
+    return lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+                             float(scale), int(bool(causal)), int(tile_order), _stream(stream))
+
+
+def attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, num_splits, max_seqlen,
+                workspace=None, workspace_bytes=0, stream=None) -> int:
+    return lib().attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), B, Hq,
+                             Hkv, d, float(scale), int(num_splits), int(max_seqlen),
+                             _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def attn_decode_workspace_bytes(B, Hq, d, num_splits) -> int:
+    return int(lib().attn_decode_workspace_bytes(B, Hq, d, num_splits))
+
+
+def attn_decode_num_splits(B, Hq, Hkv, max_seqlen) -> int:
+    return int(lib().attn_decode_num_splits(B, Hq, Hkv, max_seqlen))
+
+
+def attn_tile_map(tile_order, B, Hq, N, causal, unit):
+    b, h, m = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = lib().attn_tile_map(int(tile_order), B, Hq, N, int(bool(causal)), int(unit),
+                             ctypes.byref(b), ctypes.byref(h), ctypes.byref(m))
+    check(rc, "attn_tile_map")
+    return b.value, h.value, m.value
+
+
+def attn_fwd_units(B, Hq, N) -> int:
+    return int(lib().attn_fwd_units(B, Hq, N))
+
+
+def attn_device_status(stream=None) -> int:
+    return lib().attn_device_status(_stream(stream))
+
+
+def attn_set_wait_timeout_ns(ns: int) -> int:
+    return int(lib().attn_set_wait_timeout_ns(int(ns)))
+
+
+def attn_version() -> int:
+    return int(lib().attn_version())
+
+
+# ----------------------------------------------------------- torch helpers
+def forward(q, k, v, causal=False, scale=None, tile_order=ORDER_HEAD_FIRST, with_lse=True,
+            stream=None):
+    """Allocate outputs and run attn_fwd_ex on ``[B, H, N, d]`` bf16 CUDA tensors."""
+    import torch
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if with_lse else None
+    check(attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, stream),
+          "attn_fwd_ex")
+    return o, lse
+
+
+def decode(q, kcache, vcache, seqlens, num_splits=0, scale=None, workspace=None, stream=None):
+    """Allocate the output (and a workspace when none is given) and run attn_decode."""
+    import torch
+    B, Hq, d = q.shape
+    Hkv, s_max = kcache.shape[1], kcache.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    splits = num_splits if num_splits > 0 else attn_decode_num_splits(B, Hq, Hkv, s_max)
+    nbytes = attn_decode_workspace_bytes(B, Hq, d, splits)
+    if workspace is None and nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    check(attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, splits, s_max,
+                      workspace, nbytes, stream), "attn_decode")
+    return o, workspace, splits

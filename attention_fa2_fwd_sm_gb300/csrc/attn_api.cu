@@ -1,0 +1,239 @@
+// attn_api.cu -- the extern "C" boundary of libattn.so: argument validation
+// (entirely on the host, before any CUDA call), dispatch to the kernels,
+// device status reporting and the host-side view of the scheduler.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+#include "tile_order.cuh"
+
+namespace attn {
+
+namespace {
+
+std::atomic<long long> g_wait_ns{10LL * 1000 * 1000 * 1000};  // 10 s
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int current_num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    static int cached[64] = {0};
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return -1;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxSplits = 256;
+constexpr int kDecodeMaxGroup = 16;
+
+}  // namespace
+
+bool encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                    uint32_t box0, uint32_t box1) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {dim0, dim1, dim2};
+    const cuuint64_t strides[2] = {dim0 * 2, dim0 * dim1 * 2};
+    const cuuint32_t box[3] = {box0, box1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char *attn_strerror(int code) {
+    switch (code) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_ARG: return "invalid argument (null/misaligned pointer, bad size, Hq % Hkv, scale)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension or group size";
+        case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case ATTN_ERR_CUDA: return "CUDA runtime or driver call failed";
+        case ATTN_ERR_TIMEOUT: return "a bounded device wait ran out";
+        default: return "unknown status code";
+    }
+}
+
+long long attn_set_wait_timeout_ns(long long ns) {
+    if (ns < 0) ns = 0;
+    return g_wait_ns.exchange(ns);
+}
+
+long long attn_fwd_units(int B, int Hq, int N) {
+    if (B <= 0 || Hq <= 0 || N <= 0) return 0;
+    return (long long)B * Hq * unit_blocks(N);
+}
+
+int attn_tile_map(int tile_order, int B, int Hq, int N, int causal, long long unit, int *b, int *h,
+                  int *m) {
+    if (!b || !h || !m || B <= 0 || Hq <= 0 || N <= 0) return ATTN_ERR_ARG;
+    if (tile_order < kHeadFirst || tile_order > kNaiveHeadFirst) return ATTN_ERR_ARG;
+    const long long total = attn_fwd_units(B, Hq, N);
+    if (unit < 0 || unit >= total) return ATTN_ERR_ARG;
+    const Tile t = unit_to_tile(tile_order, unit, Hq, unit_blocks(N), causal ? 1 : 0);
+    *b = t.b;
+    *h = t.h;
+    *m = t.m;
+    return ATTN_OK;
+}
+
+static int validate_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                        int Hq, int Hkv, int N, int d, float scale, int tile_order) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0) return ATTN_ERR_ARG;
+    if (Hq % Hkv) return ATTN_ERR_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_ARG;
+    if (tile_order < kHeadFirst || tile_order > kNaiveHeadFirst) return ATTN_ERR_ARG;
+    if (d != 56 && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    // tensor-map limits: each dimension < 2^32, strides < 2^40 bytes
+    if ((long long)B * Hq >= (1LL << 31) || (long long)N * d * 2 >= (1LL << 39)) return ATTN_ERR_ARG;
+    return ATTN_OK;
+}
+
+int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                int Hkv, int N, int d, float scale, int causal, int tile_order,
+                attn_stream_t stream) {
+    int rc = validate_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, tile_order);
+    if (rc != ATTN_OK) return rc;
+    const int sms = current_num_sms();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    FwdLaunch a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.order = tile_order;
+    a.wait_ns = (unsigned long long)g_wait_ns.load();
+    a.num_sms = sms;
+    return fwd_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+             int Hkv, int N, int d, float scale, int causal, attn_stream_t stream) {
+    return attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, ATTN_ORDER_HEAD_FIRST,
+                       stream);
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int d, int num_splits) {
+    if (B <= 0 || Hq <= 0 || d <= 0 || num_splits <= 1) return 0;
+    const size_t parts = (size_t)B * Hq * num_splits;
+    size_t o_bytes = parts * d * sizeof(float);
+    o_bytes = (o_bytes + 255) / 256 * 256;
+    return o_bytes + parts * sizeof(float);
+}
+
+static int splits_for(int B, int Hkv, int max_seqlen, int sms) {
+    const long long ctas = (long long)B * Hkv;
+    long long s = (2LL * sms + ctas - 1) / ctas;
+    const long long by_len = (max_seqlen + 255) / 256;
+    if (s > by_len) s = by_len;
+    if (s > kMaxSplits) s = kMaxSplits;
+    if (s < 1) s = 1;
+    return int(s);
+}
+
+int attn_decode_num_splits(int B, int Hq, int Hkv, int max_seqlen) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || max_seqlen < 0 || Hq % Hkv) return ATTN_ERR_ARG;
+    const int sms = current_num_sms();
+    if (sms <= 0) return ATTN_ERR_CUDA;
+    return splits_for(B, Hkv, max_seqlen, sms);
+}
+
+int attn_decode(const void *q, const void *kcache, const void *vcache, const int *seqlens, void *o,
+                int B, int Hq, int Hkv, int d, float scale, int num_splits, int max_seqlen,
+                void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !seqlens ||
+        (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+        return ATTN_ERR_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || max_seqlen <= 0 || Hq % Hkv) return ATTN_ERR_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_ARG;
+    if (num_splits > kMaxSplits) return ATTN_ERR_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (Hq / Hkv > kDecodeMaxGroup) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || Hkv > 65535 || (long long)max_seqlen * d * 2 >= (1LL << 39)) return ATTN_ERR_ARG;
+    if (num_splits <= 0) {
+        const int sms = current_num_sms();
+        if (sms <= 0) return ATTN_ERR_CUDA;
+        num_splits = splits_for(B, Hkv, max_seqlen, sms);
+    }
+    const size_t need = attn_decode_workspace_bytes(B, Hq, d, num_splits);
+    if (need > 0 && (!workspace || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 15u)))
+        return ATTN_ERR_WORKSPACE;
+    DecodeLaunch a;
+    a.q = q;
+    a.kcache = kcache;
+    a.vcache = vcache;
+    a.seqlens = seqlens;
+    a.o = o;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.max_seqlen = max_seqlen;
+    a.num_splits = num_splits;
+    a.scale = scale;
+    const size_t parts = (size_t)B * Hq * num_splits;
+    size_t o_bytes = (parts * d * sizeof(float) + 255) / 256 * 256;
+    a.ws_o = need ? reinterpret_cast<float *>(workspace) : nullptr;
+    a.ws_lse = need ? reinterpret_cast<float *>(reinterpret_cast<char *>(workspace) + o_bytes) : nullptr;
+    a.wait_ns = (unsigned long long)g_wait_ns.load();
+    return decode_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_device_status(attn_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    int a = 0, b = 0;
+    if (fwd_take_status(&a) != cudaSuccess || decode_take_status(&b) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    return (a | b) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+}  // extern "C"

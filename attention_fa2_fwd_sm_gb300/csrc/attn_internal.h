@@ -1,0 +1,48 @@
+// attn_internal.h -- interfaces between the C-ABI layer and the kernel
+// translation units (not part of the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+struct FwdLaunch {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    int B, Hq, Hkv, N, d;
+    float scale;
+    int causal, order;
+    unsigned long long wait_ns;
+    int num_sms;
+};
+
+struct DecodeLaunch {
+    const void *q, *kcache, *vcache;
+    const int *seqlens;
+    void *o;
+    int B, Hq, Hkv, d, max_seqlen, num_splits;
+    float scale;
+    float *ws_o, *ws_lse;  // partial outputs / log-sum-exps (used when splits > 1)
+    unsigned long long wait_ns;
+};
+
+// Each returns 0 or a negative ATTN_ERR_* code.
+int fwd_launch(const FwdLaunch &a, cudaStream_t stream);
+int decode_launch(const DecodeLaunch &a, cudaStream_t stream);
+
+// Read and clear the status word of each kernel translation unit (OR of
+// kStatus* bits).
+cudaError_t fwd_take_status(int *bits);
+cudaError_t decode_take_status(int *bits);
+
+// Tiled bf16 tensor map over a 3-D row-major tensor [dim2][dim1][dim0]
+// (dim0 contiguous), box {box0, box1, 1}, 128-byte swizzle, zero fill out of
+// bounds.  Returns false if the driver rejects it.
+bool encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint64_t dim1,
+                    uint64_t dim2, uint32_t box0, uint32_t box1);
+
+}  // namespace attn

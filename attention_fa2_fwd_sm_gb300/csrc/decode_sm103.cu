@@ -1,0 +1,412 @@
+// decode_sm103.cu -- split-KV grouped-query decode (one query row per query
+// head) and the log-sum-exp merge of the per-split partial states.
+//
+// kernbench2 "Fused Grouped-Query Attention": a decode step processes a
+// single query position against the whole KV history, so its time is the
+// time to stream the KV cache from HBM; each KV head is shared by a group of
+// G query heads; the KV sequence is split and the running softmax states
+// (m, l, O) of the pieces are reduced (section "Inference with Long-Context
+// Length", Case 4).  Here the pieces are CTAs of one GPU and the reduction is
+// a second kernel.
+//
+// Decode CTA = (split s, KV head g, batch b); 4 consumer warps + 1 TMA warp.
+// The chunk of keys [lo, hi) of the split streams through a ring of 64-key
+// stages (K and V tiles, 128-byte swizzled, loaded by TMA).  Each consumer
+// warp takes 16 keys of a stage and computes, for the G <= 16 query heads of
+// the group at once, S = Q K^T and O += P V with m16n8k16 bf16 MMAs (query
+// heads on the M dimension), keeping its own online-softmax state.  At the
+// end the four warp states are combined through shared memory into the
+// split's partial (O_s normalised, lse_s), or into O directly when there is a
+// single split.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+static __device__ int g_decode_status;
+
+namespace dec {
+
+constexpr int kKeysPerStage = 64;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxGroup = 16;
+constexpr int kChunkGranule = 64;
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kChunkBytes = kKeysPerStage * 128;      // 64 keys x 128 bytes
+    static constexpr int kTileBytes = kKeysPerStage * D * 2;     // one K or V tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStages = (D == 128) ? 3 : 6;
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kCombineBytes = kConsumerWarps * (kMaxGroup * D + 2 * kMaxGroup) * 4;
+    static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
+    static constexpr int kNumBars = 2 * kStages;
+    static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 16 + 1024;
+};
+
+struct Params {
+    const __nv_bfloat16 *q;
+    const int *seqlens;
+    __nv_bfloat16 *o;
+    float *ws_o, *ws_lse;
+    int Hq, Hkv, G, max_seqlen, num_splits;
+    float scale_log2;
+    unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// Byte address of the 16-byte unit `u` (elements 8u..8u+7) of key row `k` of a
+// 64-key tile stored as D/64 chunks of 128-byte rows with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t tile_unit_addr(uint32_t tile, int k, int u) {
+    return tile + (u >> 3) * (kKeysPerStage * 128) + k * 128 + (((u & 7) ^ (k & 7)) << 4);
+}
+
+// Zero the bf16 halves of a V fragment register whose keys lie at or beyond
+// `n_valid` (keys k_lo and k_lo + 1 live in the low and high halves).
+__device__ __forceinline__ uint32_t mask_pair(uint32_t r, int k_lo, int n_valid) {
+    if (k_lo >= n_valid) r &= 0xffff0000u;
+    if (k_lo + 1 >= n_valid) r &= 0x0000ffffu;
+    return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const Params p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kDataBytes);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + C::kNumBars);
+    int *status = &g_decode_status;
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    int seqlen = p.seqlens[b];
+    seqlen = seqlen < 0 ? 0 : (seqlen > p.max_seqlen ? p.max_seqlen : seqlen);
+    int per = (seqlen + p.num_splits - 1) / p.num_splits;
+    const int chunk = (per + kChunkGranule - 1) / kChunkGranule * kChunkGranule;
+    const int lo = min(split * chunk, seqlen);
+    const int hi = min(lo + chunk, seqlen);
+    const int ntiles = (hi - lo + kKeysPerStage - 1) / kKeysPerStage;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(bars + s), 1);                          // full
+            mbar_init(smem_u32(bars + C::kStages + s), kConsumerWarps);  // empty
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // Per-warp online-softmax state for rows (query heads) r = lane/4 and r + 8.
+    float m_st[2] = {-INFINITY, -INFINITY};
+    float l_st[2] = {0.f, 0.f};
+    float acc[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
+
+    int issued = 0;  // tiles whose copies were issued (producer lane only)
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            for (int i = 0; i < ntiles; ++i) {
+                const int s = i % C::kStages;
+                const int round = i / C::kStages;
+                if (round > 0 && !mbar_wait_bounded(smem_u32(bars + C::kStages + s), (round - 1) & 1,
+                                                    p.wait_ns, abort_flag, status))
+                    break;
+                const uint32_t fb = smem_u32(bars + s);
+                mbar_arrive_expect_tx(fb, C::kStageBytes);
+                const uint32_t kt = smem_u32(smem + s * C::kStageBytes);
+                const int key0 = lo + i * kKeysPerStage;
+                const int plane = b * p.Hkv + g;
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(kt + c * C::kChunkBytes, &tmK, fb, c * 64, key0, plane);
+                    tma_load_3d(kt + C::kTileBytes + c * C::kChunkBytes, &tmV, fb, c * 64, key0, plane);
+                }
+                issued = i + 1;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumer
+        const int gq = lane >> 2, tq = lane & 3;
+        // Q fragments (A operand, rows = query heads of the group, k = head dim).
+        uint32_t qa[D / 16][4];
+        const int h0 = g * p.G;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int row = gq + ((i & 1) ? 8 : 0);
+                const int col = ks * 16 + tq * 2 + ((i & 2) ? 8 : 0);
+                uint32_t v = 0;
+                if (row < p.G)
+                    v = *reinterpret_cast<const uint32_t *>(p.q + ((size_t)(b * p.Hq + h0 + row)) * D + col);
+                qa[ks][i] = v;
+            }
+        }
+        const float sl2 = p.scale_log2;
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % C::kStages;
+            if (!mbar_wait_warp(smem_u32(bars + s), (i / C::kStages) & 1, p.wait_ns, abort_flag, status))
+                break;
+            const int kw = lo + i * kKeysPerStage + warp * 16;  // first key of this warp
+            const int n_valid = min(16, hi - kw);
+            if (n_valid > 0) {
+                const uint32_t kt = smem_u32(smem + s * C::kStageBytes);
+                const uint32_t vt = kt + C::kTileBytes;
+                float sc[2][4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[h][e] = 0.f;
+                {
+                    const int sub = lane >> 3, rr = lane & 7;
+                    const int key = warp * 16 + ((sub & 2) ? 8 : 0) + rr;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(tile_unit_addr(kt, key, 2 * ks + (sub & 1)), b0, b1, b2, b3);
+                        mma_bf16_16816(sc[0], qa[ks], b0, b1);
+                        mma_bf16_16816(sc[1], qa[ks], b2, b3);
+                    }
+                }
+                // scores in log2 units, masked past the chunk end
+                float x[2][4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int kl = h * 8 + tq * 2 + (e & 1);
+                        x[h][e] = kl < n_valid ? sc[h][e] * sl2 : -INFINITY;
+                    }
+                uint32_t pa[4];
+                float corr[2];
+#pragma unroll
+                for (int rsel = 0; rsel < 2; ++rsel) {  // rows gq (e = 0,1) and gq + 8 (e = 2,3)
+                    float mx = fmaxf(fmaxf(x[0][2 * rsel], x[0][2 * rsel + 1]),
+                                     fmaxf(x[1][2 * rsel], x[1][2 * rsel + 1]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float m_new = fmaxf(m_st[rsel], mx);
+                    corr[rsel] = m_new == -INFINITY ? 1.f : fast_exp2(m_st[rsel] - m_new);  // 0 when the old max is -inf
+                    m_st[rsel] = m_new;
+                    const float nm = m_new == -INFINITY ? 0.f : -m_new;
+                    const float p00 = fast_exp2(x[0][2 * rsel] + nm), p01 = fast_exp2(x[0][2 * rsel + 1] + nm);
+                    const float p10 = fast_exp2(x[1][2 * rsel] + nm), p11 = fast_exp2(x[1][2 * rsel + 1] + nm);
+                    l_st[rsel] = l_st[rsel] * corr[rsel] + (p00 + p01 + p10 + p11);
+                    pa[rsel] = pack_bf16x2(p00, p01);      // a0 (row gq) / a1 (row gq+8), keys 2tq..
+                    pa[2 + rsel] = pack_bf16x2(p10, p11);  // a2 / a3, keys 8+2tq..
+                }
+#pragma unroll
+                for (int n = 0; n < D / 8; ++n) {
+                    acc[n][0] *= corr[0];
+                    acc[n][1] *= corr[0];
+                    acc[n][2] *= corr[1];
+                    acc[n][3] *= corr[1];
+                }
+                {
+                    const int sub = lane >> 3, rr = lane & 7;
+                    const int key = warp * 16 + ((sub & 1) ? 8 : 0) + rr;
+#pragma unroll
+                    for (int nt = 0; nt < D / 16; ++nt) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(tile_unit_addr(vt, key, 2 * nt + (sub >> 1)), b0, b1, b2, b3);
+                        if (n_valid < 16) {
+                            b0 = mask_pair(b0, 2 * tq, n_valid);
+                            b1 = mask_pair(b1, 8 + 2 * tq, n_valid);
+                            b2 = mask_pair(b2, 2 * tq, n_valid);
+                            b3 = mask_pair(b3, 8 + 2 * tq, n_valid);
+                        }
+                        mma_bf16_16816(acc[2 * nt], pa, b0, b1);
+                        mma_bf16_16816(acc[2 * nt + 1], pa, b2, b3);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(bars + C::kStages + s));
+        }
+    }
+
+    // ------------------------------------------------ combine the four warps
+    __syncthreads();
+    if (*abort_flag) {
+        // A wait ran out somewhere.  Before the CTA exits, wait (bounded, with
+        // a fixed limit) for the copies of the last fill of every ring slot so
+        // that none is still writing shared memory; outputs stay unwritten.
+        if (warp == kConsumerWarps && lane == 0) {
+            volatile int no_abort = 0;
+            for (int i = max(0, issued - C::kStages); i < issued; ++i)
+                if (!mbar_wait_bounded(smem_u32(bars + i % C::kStages), (i / C::kStages) & 1,
+                                       1000000000ull, &no_abort, status))
+                    atomicOr(status, kStatusDrainTimeout);
+        }
+        return;
+    }
+    // Every issued tile was consumed: the ring can be reused for the combine.
+    float *cw = reinterpret_cast<float *>(smem);  // [warp][16][D] O, then [warp][16] m, [warp][16] l
+    float *cm = cw + kConsumerWarps * kMaxGroup * D;
+    float *cl = cm + kConsumerWarps * kMaxGroup;
+    if (warp < kConsumerWarps) {
+        const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+        for (int rsel = 0; rsel < 2; ++rsel) {
+            float l = l_st[rsel];
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            l_st[rsel] = l;
+        }
+        float *ow = cw + warp * kMaxGroup * D;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+            const int col = n * 8 + tq * 2;
+            ow[gq * D + col] = acc[n][0];
+            ow[gq * D + col + 1] = acc[n][1];
+            ow[(gq + 8) * D + col] = acc[n][2];
+            ow[(gq + 8) * D + col + 1] = acc[n][3];
+        }
+        if (tq == 0) {
+            cm[warp * kMaxGroup + gq] = m_st[0];
+            cm[warp * kMaxGroup + gq + 8] = m_st[1];
+            cl[warp * kMaxGroup + gq] = l_st[0];
+            cl[warp * kMaxGroup + gq + 8] = l_st[1];
+        }
+    }
+    __syncthreads();
+    const int G = p.G;
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const int row = idx / D, col = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * kMaxGroup + row]);
+        float wsum = 0.f, osum = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float f = fast_exp2(cm[w * kMaxGroup + row] - M);
+                wsum += f * cl[w * kMaxGroup + row];
+                osum += f * cw[(w * kMaxGroup + row) * D + col];
+            }
+        }
+        const float o = wsum > 0.f ? osum / wsum : 0.f;
+        const int h = g * G + row;
+        if (p.num_splits == 1) {
+            p.o[(size_t)(b * p.Hq + h) * D + col] = __float2bfloat16_rn(o);
+        } else {
+            const size_t pi = (size_t)(b * p.Hq + h) * p.num_splits + split;
+            p.ws_o[pi * D + col] = o;
+            if (col == 0) p.ws_lse[pi] = wsum > 0.f ? (M + __log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+}
+
+// Merge: L = max_s lse_s, w_s = exp(lse_s - L), O = sum_s w_s O_s / sum_s w_s.
+template <int D>
+__global__ void __launch_bounds__(D) merge_kernel(const float *ws_o, const float *ws_lse,
+                                                  __nv_bfloat16 *o, int num_splits) {
+    const int bh = blockIdx.x, col = threadIdx.x;
+    const float *lse = ws_lse + (size_t)bh * num_splits;
+    const float *po = ws_o + (size_t)bh * num_splits * D;
+    float L = -INFINITY;
+    for (int s = 0; s < num_splits; ++s) L = fmaxf(L, lse[s]);
+    float wsum = 0.f, acc = 0.f;
+    if (L != -INFINITY) {
+        for (int s = 0; s < num_splits; ++s) {
+            const float w = __expf(lse[s] - L);
+            wsum += w;
+            acc += w * po[(size_t)s * D + col];
+        }
+    }
+    o[(size_t)bh * D + col] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+}
+
+template <int D>
+int launch(const DecodeLaunch &a, cudaStream_t stream) {
+    using C = Cfg<D>;
+    CUtensorMap mk, mv;
+    if (!encode_bf16_3d(&mk, a.kcache, D, uint64_t(a.max_seqlen), uint64_t(a.B) * a.Hkv, 64,
+                        kKeysPerStage) ||
+        !encode_bf16_3d(&mv, a.vcache, D, uint64_t(a.max_seqlen), uint64_t(a.B) * a.Hkv, 64,
+                        kKeysPerStage))
+        return -4;
+    Params p;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+    p.seqlens = a.seqlens;
+    p.o = reinterpret_cast<__nv_bfloat16 *>(a.o);
+    p.ws_o = a.ws_o;
+    p.ws_lse = a.ws_lse;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.max_seqlen = a.max_seqlen;
+    p.num_splits = a.num_splits;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.wait_ns = a.wait_ns;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess)
+            return -4;
+        attr_set = true;
+    }
+    decode_kernel<D><<<dim3(a.num_splits, a.Hkv, a.B), dim3(kThreads), C::kSmemBytes, stream>>>(mk, mv, p);
+    if (cudaGetLastError() != cudaSuccess) return -4;
+    if (a.num_splits > 1) {
+        merge_kernel<D><<<dim3(a.B * a.Hq), dim3(D), 0, stream>>>(a.ws_o, a.ws_lse, p.o, a.num_splits);
+        if (cudaGetLastError() != cudaSuccess) return -4;
+    }
+    return 0;
+}
+
+}  // namespace dec
+
+int decode_launch(const DecodeLaunch &a, cudaStream_t stream) {
+    if (a.d == 64) return dec::launch<64>(a, stream);
+    return dec::launch<128>(a, stream);
+}
+
+cudaError_t decode_take_status(int *bits) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_decode_status, sizeof(int));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(int));
+}
+
+}  // namespace attn

@@ -1,0 +1,510 @@
+// fwd_sm103.cu -- FlashAttention-2 style forward (prefill) kernel for sm_103a.
+//
+// Computes O = softmax(scale * Q K^T) V and lse per query row ("Optimizing
+// Attention on GPUs by Exploiting GPU Architectural NUMA Effects", detail
+// page, section 4 equation) with FA2's partitioning (Figure 4: each CTA owns
+// a block of query rows and streams every K/V block of its head) and an
+// online softmax (running max m, running sum l, rescaled O; kernbench2
+// "Fused Grouped-Query Attention", short-context section: running
+// accumulators (m, l, O)).
+//
+// Design (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer: Q tiles, then a ring of K/V blocks (128 keys).
+//   warp 1      tcgen05 issuer (one thread) + TMEM owner.
+//   warps 4-7   softmax / epilogue of MMA tile 0 (query rows 0-127 of the unit)
+//   warps 8-11  softmax / epilogue of MMA tile 1 (rows 128-255)
+// A unit is 256 query rows of one head: two 128-row MMA tiles share every
+// K/V block loaded into shared memory.  TMEM (512 columns): S/P of tile t at
+// columns [128 t, 128 t + 128), O of tile t at [256 + D t, 256 + D t + D).
+// S = Q K^T is an SS MMA (M=128, N=128, K=16 steps); P (bf16) is written
+// over S in TMEM and O += P V is a TS MMA with V read MN-major from shared
+// memory.  The issue order QK(t, j+1) after PV(t, j) means the commit that
+// announces S(t, j+1) also guarantees PV(t, j) is complete, so the softmax
+// warps may rescale O(t) in TMEM right after they see S(t, j+1); O is only
+// rescaled when a row's maximum grows by more than 2^8 (exactly the same
+// result up to rounding, since l and O always share the reference maximum).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+#include "tile_order.cuh"
+
+namespace attn {
+
+static __device__ int g_fwd_status;
+
+namespace fwd {
+
+constexpr int kTileM = 128;    // query rows per MMA tile
+constexpr int kBlockN = 128;   // keys per K/V block
+constexpr int kNT = 2;         // MMA tiles per unit
+constexpr int kThreads = 384;  // 12 warps
+constexpr int kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (log2 units)
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;              // 128-byte column chunks per row
+    static constexpr int kChunkBytes = 128 * 128;       // 128 rows x 128 bytes
+    static constexpr int kQBytes = kTileM * D * 2;
+    static constexpr int kKVBytes = kBlockN * D * 2;
+    static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring slots
+    static constexpr int kOCol = 2 * kTileM;            // first O column in TMEM
+    // barriers: q_full[2] q_empty[2] s_full[2] p_full[2] o_full[2] o_empty[2]
+    //           kv_full[S] kv_empty[S] drain
+    static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarSFull = 4, kBarPFull = 6,
+                         kBarOFull = 8, kBarOEmpty = 10, kBarKVFull = 12,
+                         kBarKVEmpty = 12 + kStages, kBarDrain = 12 + 2 * kStages,
+                         kNumBars = 13 + 2 * kStages;
+    static constexpr int kDataBytes = kNT * kQBytes + kStages * kKVBytes;
+    static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 16 + 1024;  // + align slack
+};
+
+struct Params {
+    __nv_bfloat16 *o;
+    float *lse;
+    int N, Hq, Hkv, G, d_store, causal, order, nb;
+    long long total_units;
+    float scale_log2;
+    unsigned long long wait_ns;
+};
+
+struct UnitWork {
+    int b, h, kvh;
+    int row0[kNT];
+    int nkv[kNT];  // K/V blocks each tile visits (0: tile lies past N)
+    int nmax;
+};
+
+__device__ __forceinline__ UnitWork unit_work(const Params &p, long long u) {
+    const Tile t = unit_to_tile(p.order, u, p.Hq, p.nb, p.causal);
+    UnitWork w;
+    w.b = t.b;
+    w.h = t.h;
+    w.kvh = t.h / p.G;
+    const int nkv_all = (p.N + kBlockN - 1) / kBlockN;
+    w.nmax = 0;
+#pragma unroll
+    for (int tt = 0; tt < kNT; ++tt) {
+        const int r0 = t.m * kUnitRows + tt * kTileM;
+        w.row0[tt] = r0;
+        int n = 0;
+        if (r0 < p.N) n = p.causal ? min(nkv_all, r0 / kBlockN + 1) : nkv_all;
+        w.nkv[tt] = n;
+        w.nmax = max(w.nmax, n);
+    }
+    return w;
+}
+
+// Last tile (highest index) that still uses K/V block j.
+__device__ __forceinline__ int last_user(const UnitWork &w, int j) {
+    int last = -1;
+#pragma unroll
+    for (int t = 0; t < kNT; ++t)
+        if (j < w.nkv[t]) last = t;
+    return last;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sKV = smem + kNT * C::kQBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kDataBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < kNT; ++t) {
+            mbar_init(bar(C::kBarQFull + t), 1);
+            mbar_init(bar(C::kBarQEmpty + t), 1);
+            mbar_init(bar(C::kBarSFull + t), 1);
+            mbar_init(bar(C::kBarPFull + t), kTileM);
+            mbar_init(bar(C::kBarOFull + t), 1);
+            mbar_init(bar(C::kBarOEmpty + t), kTileM);
+        }
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar(C::kBarKVFull + s), 1);
+            mbar_init(bar(C::kBarKVEmpty + s), 1);
+        }
+        mbar_init(bar(C::kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const bool persistent = p.order != kNaiveHeadFirst;
+    const long long u_step = persistent ? (long long)gridDim.x : p.total_units;
+    int *status = &g_fwd_status;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            long long fills = 0;          // K/V ring fills issued
+            int q_loads[kNT] = {0, 0};    // Q loads issued per tile
+            bool ok = true;
+            for (long long u = blockIdx.x; ok && u < p.total_units; u += u_step) {
+                const UnitWork w = unit_work(p, u);
+                for (int t = 0; t < kNT && ok; ++t) {
+                    if (w.nkv[t] == 0) continue;
+                    if (q_loads[t] > 0)
+                        ok = mbar_wait_bounded(bar(C::kBarQEmpty + t), (q_loads[t] - 1) & 1,
+                                               p.wait_ns, abort_flag, status);
+                    if (!ok) break;
+                    const uint32_t qb = bar(C::kBarQFull + t);
+                    mbar_arrive_expect_tx(qb, C::kQBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(smem_u32(sQ + t * C::kQBytes + c * C::kChunkBytes), &tmQ, qb,
+                                    c * 64, w.row0[t], w.b * p.Hq + w.h);
+                    ++q_loads[t];
+                }
+                for (int j = 0; ok && j < w.nmax; ++j) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const int slot = int(fills % C::kStages);
+                        const long long round = fills / C::kStages;
+                        if (round > 0) {
+                            ok = mbar_wait_bounded(bar(C::kBarKVEmpty + slot), uint32_t((round - 1) & 1),
+                                                   p.wait_ns, abort_flag, status);
+                            if (!ok) break;
+                        }
+                        const uint32_t fb = bar(C::kBarKVFull + slot);
+                        mbar_arrive_expect_tx(fb, C::kKVBytes);
+                        const CUtensorMap *map = kv == 0 ? &tmK : &tmV;
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(smem_u32(sKV + slot * C::kKVBytes + c * C::kChunkBytes), map,
+                                        fb, c * 64, j * kBlockN, w.b * p.Hkv + w.kvh);
+                        ++fills;
+                    }
+                }
+            }
+            if (!ok) {
+                // Drain: wait (bounded, independent of the caller's limit) for the
+                // last fill of every slot and the last Q load of every tile, so no
+                // copy is still writing shared memory when the CTA exits.
+                const unsigned long long drain_ns = 1000000000ull;
+                volatile int no_abort = 0;
+                for (int s = 0; s < C::kStages; ++s) {
+                    long long last = fills - 1 - ((fills - 1 - s) % C::kStages + C::kStages) % C::kStages;
+                    if (fills == 0 || last < 0) continue;
+                    if (!mbar_wait_bounded(bar(C::kBarKVFull + int(last % C::kStages)),
+                                           uint32_t((last / C::kStages) & 1), drain_ns, &no_abort,
+                                           status))
+                        atomicOr(status, kStatusDrainTimeout);
+                }
+                for (int t = 0; t < kNT; ++t)
+                    if (q_loads[t] > 0 &&
+                        !mbar_wait_bounded(bar(C::kBarQFull + t), (q_loads[t] - 1) & 1, drain_ns,
+                                           &no_abort, status))
+                        atomicOr(status, kStatusDrainTimeout);
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescQK = idesc_bf16_f32(kTileM, kBlockN, 0);
+            constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileM, D, 1);
+            long long fills = 0;                 // ring position of the next block used
+            int q_used[kNT] = {0, 0};            // Q loads consumed per tile
+            int p_waits[kNT] = {0, 0};           // P(t) handoffs consumed
+            int units_done[kNT] = {0, 0};        // epilogues owed per tile
+            bool ok = true;
+
+            auto wait_slot = [&](long long f) {
+                return mbar_wait_bounded(bar(C::kBarKVFull + int(f % C::kStages)),
+                                         uint32_t((f / C::kStages) & 1), p.wait_ns, abort_flag, status);
+            };
+            auto slot_addr = [&](long long f) {
+                return smem_u32(sKV + int(f % C::kStages) * C::kKVBytes);
+            };
+            auto issue_qk = [&](int t, long long fK) {
+                const uint32_t qa = smem_u32(sQ + t * C::kQBytes);
+                const uint32_t ka = slot_addr(fK);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+                    tc_mma_ss(tmem_base + t * kTileM, smem_desc_sw128(qa + off, 16, 1024),
+                              smem_desc_sw128(ka + off, 16, 1024), kIdescQK, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int t, long long fV, bool acc) {
+                const uint32_t va = slot_addr(fV);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    tc_mma_ts(tmem_base + C::kOCol + t * D, tmem_base + t * kTileM + kk * 8,
+                              smem_desc_sw128(va + kk * 16 * 128, C::kChunkBytes, 1024), kIdescPV,
+                              (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            for (long long u = blockIdx.x; ok && u < p.total_units; u += u_step) {
+                const UnitWork w = unit_work(p, u);
+                const long long f0 = fills;  // K_j at f0 + 2j, V_j at f0 + 2j + 1
+                // prologue: S(t, 0) = Q(t) K_0^T
+                ok = wait_slot(f0);
+                for (int t = 0; ok && t < kNT; ++t) {
+                    if (w.nkv[t] == 0) continue;
+                    ok = mbar_wait_bounded(bar(C::kBarQFull + t), q_used[t] & 1, p.wait_ns,
+                                           abort_flag, status);
+                    if (!ok) break;
+                    ++q_used[t];
+                    tc_fence_after();
+                    issue_qk(t, f0);
+                    tc_commit(bar(C::kBarSFull + t));
+                    if (t == last_user(w, 0)) tc_commit(bar(C::kBarKVEmpty + int(f0 % C::kStages)));
+                }
+                for (int j = 0; ok && j < w.nmax; ++j) {
+                    const long long fV = f0 + 2 * j + 1, fK = f0 + 2 * j + 2;
+                    bool v_ready = false, k_ready = false;
+                    for (int t = 0; ok && t < kNT; ++t) {
+                        if (j >= w.nkv[t]) continue;
+                        ok = mbar_wait_bounded(bar(C::kBarPFull + t), p_waits[t] & 1, p.wait_ns,
+                                               abort_flag, status);
+                        if (!ok) break;
+                        ++p_waits[t];
+                        if (j == 0 && units_done[t] > 0) {
+                            ok = mbar_wait_bounded(bar(C::kBarOEmpty + t), (units_done[t] - 1) & 1,
+                                                   p.wait_ns, abort_flag, status);
+                            if (!ok) break;
+                        }
+                        if (!v_ready) {
+                            ok = wait_slot(fV);
+                            if (!ok) break;
+                            v_ready = true;
+                        }
+                        tc_fence_after();
+                        issue_pv(t, fV, j > 0);
+                        if (t == last_user(w, j)) tc_commit(bar(C::kBarKVEmpty + int(fV % C::kStages)));
+                        if (j + 1 < w.nkv[t]) {
+                            if (!k_ready) {
+                                ok = wait_slot(fK);
+                                if (!ok) break;
+                                k_ready = true;
+                            }
+                            issue_qk(t, fK);
+                            tc_commit(bar(C::kBarSFull + t));
+                            if (t == last_user(w, j + 1))
+                                tc_commit(bar(C::kBarKVEmpty + int(fK % C::kStages)));
+                        } else {
+                            tc_commit(bar(C::kBarOFull + t));   // O(t) final for this unit
+                            tc_commit(bar(C::kBarQEmpty + t));  // Q(t) buffer reusable
+                            ++units_done[t];
+                        }
+                    }
+                }
+                fills = f0 + 2 * (long long)w.nmax;
+            }
+            // Teardown: make sure every issued MMA has finished before TMEM is freed.
+            tc_commit(bar(C::kBarDrain));
+            volatile int no_abort = 0;
+            if (!mbar_wait_bounded(bar(C::kBarDrain), 0, 1000000000ull, &no_abort, status))
+                atomicOr(status, kStatusDrainTimeout);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------- softmax / epilogue
+        const int t = (warp - 4) >> 2;      // MMA tile of this warpgroup
+        const int quarter = warp & 3;       // TMEM lane quarter of this warp
+        const int r = quarter * 32 + lane;  // row inside the tile
+        const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        const uint32_t tS = tmem_base + lane_off + t * kTileM;
+        const uint32_t tO = tmem_base + lane_off + C::kOCol + t * D;
+        const float sl2 = p.scale_log2;
+        int s_waits = 0, o_waits = 0;
+        bool ok = true;
+
+        for (long long u = blockIdx.x; ok && u < p.total_units; u += u_step) {
+            const UnitWork w = unit_work(p, u);
+            const int nkv = w.nkv[t];
+            if (nkv == 0) continue;
+            const int row = w.row0[t] + r;
+            float m_run = -INFINITY, l_run = 0.f;
+
+            for (int j = 0; j < nkv; ++j) {
+                ok = mbar_wait_warp(bar(C::kBarSFull + t), s_waits & 1, p.wait_ns, abort_flag,
+                                    status);
+                if (!ok) break;
+                ++s_waits;
+                tc_fence_after();
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+                tmem_wait_ld();
+                float s[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+
+                const int kv0 = j * kBlockN;
+                const bool ragged = kv0 + kBlockN > p.N;
+                const bool diag = p.causal && (kv0 + kBlockN - 1 > w.row0[t]);
+                if (ragged || diag) {
+                    int lim = p.N - kv0;
+                    if (p.causal) lim = min(lim, row + 1 - kv0);
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= lim) s[c] = -INFINITY;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+                const float m_new = fmaxf(m_run, mx * sl2);
+                float corr = 1.f;
+                if (m_new > m_run + kRescaleLog2) {
+                    corr = fast_exp2(m_run - m_new);  // 0 when m_run = -inf
+                    m_run = m_new;
+                }
+                l_run *= corr;
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+
+                // P = 2^(s*scale*log2e - m) in bf16, written over S in TMEM.
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = fast_exp2(fmaf(s[c * 32 + 2 * i], sl2, neg_m));
+                        const float p1 = fast_exp2(fmaf(s[c * 32 + 2 * i + 1], sl2, neg_m));
+                        l_run += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tS + c * 16, pk);
+                }
+                // Rescale this row of O when its reference maximum moved (never on
+                // the first block: PV(t, 0) overwrites O).
+                if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + c * 32, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
+                        tmem_st32(tO + c * 32, ov);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(C::kBarPFull + t));
+            }
+            if (!ok) break;
+
+            // Epilogue: O / l -> bf16, lse = (m + log2 l) * ln 2.
+            ok = mbar_wait_warp(bar(C::kBarOFull + t), o_waits & 1, p.wait_ns, abort_flag, status);
+            if (!ok) break;
+            ++o_waits;
+            tc_fence_after();
+            const float inv_l = 1.f / l_run;
+            const bool row_ok = row < p.N;
+            __nv_bfloat16 *orow = p.o + ((size_t)(w.b * p.Hq + w.h) * p.N + (row_ok ? row : 0)) * p.d_store;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(tO + c * 32, ov);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                                        __uint_as_float(ov[2 * i + 1]) * inv_l);
+                if (row_ok) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = c * 32 + g * 8;
+                        if (col < p.d_store)
+                            *reinterpret_cast<uint4 *>(orow + col) =
+                                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+                    }
+                }
+            }
+            if (row_ok && p.lse)
+                p.lse[(size_t)(w.b * p.Hq + w.h) * p.N + row] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+            tc_fence_before();
+            mbar_arrive(bar(C::kBarOEmpty + t));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <int D>
+int launch(const FwdLaunch &a, cudaStream_t stream) {
+    using C = Cfg<D>;
+    CUtensorMap mq, mk, mv;
+    const uint64_t dq = uint64_t(a.d);
+    if (!encode_bf16_3d(&mq, a.q, dq, uint64_t(a.N), uint64_t(a.B) * a.Hq, 64, kTileM) ||
+        !encode_bf16_3d(&mk, a.k, dq, uint64_t(a.N), uint64_t(a.B) * a.Hkv, 64, kBlockN) ||
+        !encode_bf16_3d(&mv, a.v, dq, uint64_t(a.N), uint64_t(a.B) * a.Hkv, 64, kBlockN))
+        return -4;
+    Params p;
+    p.o = reinterpret_cast<__nv_bfloat16 *>(a.o);
+    p.lse = a.lse;
+    p.N = a.N;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.d_store = a.d;
+    p.causal = a.causal ? 1 : 0;
+    p.order = a.order;
+    p.nb = unit_blocks(a.N);
+    p.total_units = (long long)a.B * a.Hq * p.nb;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.wait_ns = a.wait_ns;
+    static bool attr_set = false;  // per instantiation; the attribute is per function
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes) != cudaSuccess)
+            return -4;
+        attr_set = true;
+    }
+    long long grid = p.total_units;
+    if (a.order != kNaiveHeadFirst && grid > a.num_sms) grid = a.num_sms;
+    if (grid > 0x7fffffffLL) return -2;
+    fwd_kernel<D><<<dim3(unsigned(grid)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace fwd
+
+int fwd_launch(const FwdLaunch &a, cudaStream_t stream) {
+    if (a.d <= 64) return fwd::launch<64>(a, stream);
+    return fwd::launch<128>(a, stream);
+}
+
+cudaError_t fwd_take_status(int *bits) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_fwd_status, sizeof(int));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_fwd_status, &zero, sizeof(int));
+}
+
+}  // namespace attn

@@ -1,0 +1,54 @@
+// tile_order.cuh -- work-unit scheduler of the forward kernel (host + device).
+//
+// A unit is kUnitRows query rows of one query head of one batch entry.  The
+// order decides which units run at the same time, and hence which K/V tiles
+// the L2 cache can share between concurrently running CTAs.
+//
+// "Optimizing Attention on GPUs by Exploiting GPU Architectural NUMA
+// Effects" (detail page): an Attention Compute Cluster (ACC) is the set of
+// workgroups sharing one head's K/V (one KV group for GQA), section 2 Q2;
+// head-first runs one ACC's row blocks together, block-first runs every head
+// of one row block together (section 3 "before/after" table).  The XCD
+// placement half of the pages' swizzle has no counterpart here: the GPU's
+// L2 is coherent across its two dies (section 2 Q1), so the head-first order
+// alone keeps the ACC's CTAs together in time.
+#pragma once
+
+#include <cstdint>
+
+namespace attn {
+
+constexpr int kUnitRows = 256;  // query rows per unit (two 128-row MMA tiles)
+
+enum TileOrder : int { kHeadFirst = 0, kBlockFirst = 1, kNaiveHeadFirst = 2 };
+
+struct Tile {
+    int b, h, m;  // batch entry, query head, 256-row block index
+};
+
+__host__ __device__ inline int unit_blocks(int N) { return (N + kUnitRows - 1) / kUnitRows; }
+
+// Linear unit id -> tile.  Head-first (and naive head-first): the block index
+// runs fastest, then the query head, then the batch entry; because query
+// heads of one KV group are contiguous, a group's units are consecutive.
+// Block-first: the query head runs fastest.  Causal: blocks are visited in
+// descending order so the longest units start first.
+__host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int nb, int causal) {
+    Tile t;
+    int r;
+    if (order == kBlockFirst) {
+        t.h = int(u % Hq);
+        long long bm = u / Hq;
+        r = int(bm % nb);
+        t.b = int(bm / nb);
+    } else {
+        r = int(u % nb);
+        long long bh = u / nb;
+        t.h = int(bh % Hq);
+        t.b = int(bh / Hq);
+    }
+    t.m = causal ? (nb - 1 - r) : r;
+    return t;
+}
+
+}  // namespace attn

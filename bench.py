@@ -1,0 +1,387 @@
+"""Benchmark of the attention hot path on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+one forward (prefill) call on the MHA workload (B=1, H=128, d=128,
+N=32768, non-causal, head-first order) and one split-KV decode call on the
+GQA decode workload (B=8, Hq=64, Hkv=8, d=128, 32768 cached keys per
+sequence).  ``value`` is the forward TFLOP/s (4*B*H*N^2*d algorithmic flops
+per call / the call's CUDA-event time); the decode figures are reported in
+the ``decode`` object.  Inputs are larger than L2 (4 GiB and 1 GiB), so no
+flush is needed between steps.
+
+``--impl reference`` times the fp64 CPU oracle instead (on a bounded sample
+of the same forward workload: a number of query rows of one head), reported
+in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (% BF16 peak); GQA decode KV GB/s (% HBM) and us/step"
+FWD = dict(B=1, H=128, N=32768, d=128, causal=False)
+DEC = dict(B=8, Hq=64, Hkv=8, S=32768, d=128)
+
+
+def fwd_flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_gpu(args):
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import decode_inputs, prefill_inputs
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or ws > 1:
+        _build.build()
+    attn.lib()
+
+    B, H, N, d, causal = FWD["B"], FWD["H"], args.n, FWD["d"], FWD["causal"]
+    order = attn.ORDERS[args.order]
+    q, k, v = prefill_inputs(11, B, H, H, N, d, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(d)
+    Bd, Hq, Hkv, S, dd = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["S"], DEC["d"]
+    qd, kc, vc = decode_inputs(70, Bd, Hq, Hkv, S, dd, dev)
+    seqlens = torch.full((Bd,), S, dtype=torch.int32, device=dev)
+    splits = attn.attn_decode_num_splits(Bd, Hq, Hkv, S)
+    wbytes = attn.attn_decode_workspace_bytes(Bd, Hq, dd, splits)
+    wsp = torch.empty(max(wbytes, 16), dtype=torch.uint8, device=dev)
+    od = torch.empty_like(qd)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    dscale = 1.0 / math.sqrt(dd)
+
+    def prefill():
+        attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, H, H, N, d, scale, causal, order, sh), "attn_fwd")
+
+    def decode():
+        attn.check(attn.attn_decode(qd, kc, vc, seqlens, od, Bd, Hq, Hkv, dd, dscale, splits, S, wsp,
+                                    wbytes, sh), "attn_decode")
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        prefill()
+        decode()
+    barrier()
+    attn.check(attn.attn_device_status(sh), "warm-up status")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            prefill()
+            ev[i][1].record(stream)
+            decode()
+            ev[i][2].record(stream)
+        end.record(stream)
+        barrier()
+    attn.check(attn.attn_device_status(sh), "timed-region status")
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms, sum(fwd_ms), sum(dec_ms)], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, fwd_sum, dec_sum = t.tolist()
+    else:
+        fwd_sum, dec_sum = sum(fwd_ms), sum(dec_ms)
+
+    flops = fwd_flops(B, H, N, d, causal)
+    fwd_avg_s = fwd_sum / K / 1e3
+    value = ws * flops / fwd_avg_s / 1e12
+    peaks, peak_src = load_peaks()
+    per_gpu = flops / fwd_avg_s / 1e12
+    dec_bytes = 2 * Bd * Hkv * S * dd * 2 + 2 * Bd * Hq * dd * 2
+    dec_avg_s = dec_sum / K / 1e3
+    dec_gbs = dec_bytes / dec_avg_s / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"MHA forward B={B} H={H} N={N} d={d} non-causal, {args.order} order"
+                               f" + GQA decode B={Bd} Hq={Hq} Hkv={Hkv} S={S} d={dd}",
+                   "B": B, "H": H, "seq_len": N, "head_dim": d, "causal": causal,
+                   "tile_order": args.order, "decode_batch": Bd, "decode_kv_len": S,
+                   "decode_splits": splits, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "roofline": {"bound": "tensor", "achieved": round(per_gpu, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(per_gpu / peaks["bf16_tflops"], 4), "traffic": None,
+                     "peak_source": f"{peak_src} bf16 burst", "kernel": "fwd_kernel<128>"},
+        "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "us_per_step": round(dec_avg_s * 1e6, 2),
+                   "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4), "hbm_peak_gbs": peaks["hbm_gbs"],
+                   "bytes_per_step": dec_bytes},
+        "gpu_launches": K * (1 + (2 if splits > 1 else 1)),
+        "clocks": clk.summary(),
+    }
+
+    # -- tile-order ablation (same workload, each order timed alone) --
+    if args.ablation and rank == 0:
+        abl = {}
+        for name, oid in attn.ORDERS.items():
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, H, H, N, d, scale, causal, oid, sh), "warm")
+            reps = 3
+            e0.record(stream)
+            for _ in range(reps):
+                attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, H, H, N, d, scale, causal, oid, sh), "abl")
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / reps
+            abl[name] = {"ms": round(ms, 3), "tflops": round(flops / (ms / 1e3) / 1e12, 2)}
+        result["ablation"] = abl
+        result["gpu_launches_ablation"] = 12
+
+    # -- end to end through the C ABI with host buffers --
+    if args.e2e and rank == 0:
+        hq_, hk_, hv_ = (t.cpu().pin_memory() for t in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        reps = max(2, min(K, 5))
+
+        def e2e_step():
+            dq.copy_(hq_, non_blocking=True)
+            dk.copy_(hk_, non_blocking=True)
+            dv.copy_(hv_, non_blocking=True)
+            attn.check(attn.attn_fwd_ex(dq, dk, dv, o, lse, B, H, H, N, d, scale, causal, order, sh), "e2e")
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e2e_s = (time.perf_counter() - t0) / reps
+        result["e2e"] = {"value": round(flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+                         "h2d_bytes_per_step": 3 * q.numel() * 2,
+                         "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+                         "steps": reps, "api": "attn_fwd_ex (C ABI) with pinned host buffers"}
+        result["gpu_launches_e2e"] = reps + 1
+
+    if args.cpu_baseline and rank == 0:
+        result["cpu_baseline"] = cpu_baseline(q, k, v, scale, causal, args.cpu_seconds)
+
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def _oracle_sample_rate(q_rows, k_head, v_head, scale, causal, positions, budget_s):
+    """Time the oracle on growing row counts until the budget is spent."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    N, d = k_head.shape
+    rows_done, secs = 0, 0.0
+    step = max(threads, 16)
+    total_rows = q_rows.shape[0]
+    i = 0
+    while secs < budget_s and i < total_rows:
+        n = min(step, total_rows - i)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q_rows[i:i + n], k_head, v_head, scale, causal, positions[i:i + n])
+        secs += time.perf_counter() - t0
+        rows_done += n
+        i += n
+        step = min(step * 2, 4096)
+    flops_per_row = 4.0 * N * d
+    return rows_done, secs, rows_done * flops_per_row / secs / 1e12, threads
+
+
+def cpu_baseline(q, k, v, scale, causal, budget_s):
+    """The fp64 oracle as it stands, on rows of head 0 of the same workload."""
+    import numpy as np
+    N = q.shape[2]
+    rows = min(N, 8192)
+    positions = np.arange(rows, dtype=np.int64)
+    qh = q[0, 0, :rows].double().cpu().numpy()
+    kh = k[0, 0].double().cpu().numpy()
+    vh = v[0, 0].double().cpu().numpy()
+    n_rows, secs, tflops, threads = _oracle_sample_rate(qh, kh, vh, scale, causal, positions, budget_s)
+    return {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_rows} query rows of head 0 (N={N}, d={q.shape[3]}) in {secs:.1f} s; "
+                      f"rate extrapolated to the whole call"}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores (rank 0 only)."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import numpy as np
+    import torch
+
+    from synthetic_inputs import prefill_inputs
+    B, H, N, d, causal = FWD["B"], FWD["H"], args.n, FWD["d"], FWD["causal"]
+    # only head 0 is needed for the sample: draw the same tensors on the CPU
+    q, k, v = prefill_inputs(11, B, 1, 1, N, d, "cpu")
+    scale = 1.0 / math.sqrt(d)
+    rows = min(N, 8192)
+    qh = q[0, 0, :rows].double().numpy()
+    kh, vh = k[0, 0].double().numpy(), v[0, 0].double().numpy()
+    pos = np.arange(rows, dtype=np.int64)
+    per_step = max(1.0, args.ref_seconds)
+    for _ in range(args.warmup):
+        _oracle_sample_rate(qh, kh, vh, scale, causal, pos, per_step / 4)
+    rates, total_s, total_rows, threads = [], 0.0, 0, 1
+    for _ in range(args.steps):
+        n, s, r, threads = _oracle_sample_rate(qh, kh, vh, scale, causal, pos, per_step)
+        rates.append(r)
+        total_s += s
+        total_rows += n
+    value = statistics.mean(rates)
+    flops_call = fwd_flops(B, H, N, d, causal)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_s / args.steps * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"MHA forward B={B} H={H} N={N} d={d} non-causal (fp64 oracle, "
+                               f"sampled rows of head 0)", "B": B, "H": H, "seq_len": N,
+                   "head_dim": d, "causal": causal},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{total_rows} query rows over {args.steps} steps; a whole call "
+                                   f"({flops_call:.3g} flop) would take {flops_call / value / 1e12:.3g} s"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--n", type=int, default=FWD["N"], help="forward sequence length")
+    ap.add_argument("--order", default="head_first", choices=["head_first", "block_first",
+                                                              "naive_head_first"])
+    ap.add_argument("--no-ablation", dest="ablation", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=8.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

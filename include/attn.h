@@ -1,0 +1,164 @@
+/*
+ * attn.h -- C ABI of libattn.so: fused scaled dot-product attention for
+ * NVIDIA GB300 (sm_103a), FlashAttention-2 style, with a head-first
+ * persistent tile scheduler and a split-KV grouped-query decode.
+ *
+ * What is computed (all entry points): for each batch b, query head h and
+ * query row i,
+ *     s_j = scale * <q_i, k_j>,   P = softmax over the attended keys j,
+ *     o_i = sum_j P_j v_j,        lse_i = log(sum_j exp(s_j))  (natural log)
+ * -- the equation of "Optimizing Attention on GPUs by Exploiting GPU
+ * Architectural NUMA Effects" (detail page, section 4, "Equation physical
+ * meaning"), with the caller passing scale (normally 1/sqrt(d)).  Query head
+ * h reads KV head h / (Hq / Hkv) (contiguous groups of query heads share one
+ * KV head, as in grouped-query attention).
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named q, k, v, o, kcache, vcache, seqlens, lse and workspace
+ *    are DEVICE pointers owned by the caller, 16-byte aligned, to contiguous
+ *    row-major tensors.  The library never allocates, frees or keeps them.
+ *  - Element types: q, k, v, o, kcache, vcache are bf16; lse and the
+ *    workspace are fp32; seqlens is int32.  Arithmetic is bf16 x bf16 with
+ *    fp32 accumulation; probabilities are rounded to bf16 before the P*V
+ *    product; outputs are rounded to bf16 (round to nearest even).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Argument errors are detected on the host before any
+ *    CUDA call and leave all memory untouched.
+ *  - Return value: ATTN_OK (0) or one of the negative ATTN_ERR_* codes.
+ *    attn_strerror() gives a message for each.
+ *  - Device-side bounded waits: every spin on a barrier inside the kernels
+ *    is limited in time.  A wait that runs out sets a device status word and
+ *    the kernel returns early (its outputs are then undefined).
+ *    attn_device_status() reads and clears that word.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *attn_stream_t;
+
+enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_ARG = -1,         /* null or misaligned pointer, bad size, Hq % Hkv != 0, scale <= 0 */
+    ATTN_ERR_UNSUPPORTED = -2, /* head dimension or group size this library does not implement */
+    ATTN_ERR_WORKSPACE = -3,   /* workspace missing or smaller than attn_decode_workspace_bytes() */
+    ATTN_ERR_CUDA = -4,        /* a CUDA runtime or driver call failed (launch, tensor map, ...) */
+    ATTN_ERR_TIMEOUT = -5      /* a bounded device wait ran out (reported by attn_device_status) */
+};
+
+/* Orders in which the persistent forward kernel visits its work units (a
+ * unit = 256 query rows of one query head of one batch entry).
+ *  HEAD_FIRST: all row blocks of one Attention Compute Cluster (the query
+ *    heads sharing one KV head) before the next one, so CTAs running at the
+ *    same time read the same K/V and reuse it in L2 (detail page, section 2
+ *    Q2 and section 3 "before/after" table).  Causal units of a head run
+ *    last-block-first (longest first).
+ *  BLOCK_FIRST: all heads of one row block before the next row block (the
+ *    pages' "Naive Block-first" baseline).
+ *  NAIVE_HEAD_FIRST: head-first linear order, but one CTA per unit with the
+ *    hardware choosing placement (the pages' "Naive Head-first"). */
+enum attn_tile_order {
+    ATTN_ORDER_HEAD_FIRST = 0,
+    ATTN_ORDER_BLOCK_FIRST = 1,
+    ATTN_ORDER_NAIVE_HEAD_FIRST = 2
+};
+
+/*
+ * Forward (prefill) attention.  Detail page, section 4 equation; FA2 tiling of
+ * Figure 4 (each CTA owns a block of query rows and streams all of K and V).
+ *   q      [B, Hq,  N, d]  bf16
+ *   k, v   [B, Hkv, N, d]  bf16
+ *   o      [B, Hq,  N, d]  bf16 (written)
+ *   lse    [B, Hq,  N]     fp32 (written; may be NULL)
+ *   d in {56, 64, 128}; d = 56 is computed as 64 with zero columns, which
+ *   gives the same result as explicit zero padding (scale stays as passed).
+ *   causal != 0 keeps key j for query i iff j <= i.
+ *   B, Hq, Hkv, N >= 1; Hq % Hkv == 0; scale > 0 and finite.
+ * Uses the HEAD_FIRST order.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+             attn_stream_t stream);
+
+/* attn_fwd with an explicit tile order (enum attn_tile_order).  All orders
+ * give bit-identical results; only the schedule differs. */
+int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                int tile_order, attn_stream_t stream);
+
+/*
+ * Split-KV grouped-query decode, one query row per (batch, query head).
+ * kernbench2 "Fused Grouped-Query Attention": decode step with T_q = 1
+ * against the whole KV history; the KV sequence is split and the partial
+ * softmax states (m, l, O) are merged (section "Inference with Long-Context
+ * Length", Case 4).
+ *   q        [B, Hq, d]                bf16
+ *   kcache   [B, Hkv, max_seqlen, d]   bf16
+ *   vcache   [B, Hkv, max_seqlen, d]   bf16
+ *   seqlens  [B]  int32 device array; sequence b attends keys [0, seqlens[b]),
+ *            each value must lie in [0, max_seqlen] (not checked on device:
+ *            larger values are clamped to max_seqlen).
+ *   o        [B, Hq, d]                bf16 (written; zeros for seqlens[b] = 0)
+ *   d in {64, 128}; 1 <= Hq / Hkv <= 16.
+ *   num_splits <= 0 picks a split count (attn_decode_num_splits); otherwise
+ *   1 <= num_splits <= 256.  The key range of sequence b is cut into chunks of
+ *   ceil(seqlens[b] / num_splits) keys rounded up to 64; empty chunks are
+ *   allowed.  Different split counts agree up to fp32 rounding.
+ *   workspace: fp32 scratch of at least attn_decode_workspace_bytes(B, Hq, d,
+ *   splits) bytes (may be NULL when that is 0).  Layout: partial outputs
+ *   [B, Hq, splits, d] (each normalised by its own sum) followed by partial
+ *   log-sum-exps [B, Hq, splits] (-inf for an empty chunk).
+ * A second kernel merges the partials when splits > 1.
+ */
+int attn_decode(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                void *o, int B, int Hq, int Hkv, int d, float scale, int num_splits,
+                int max_seqlen, void *workspace, size_t workspace_bytes,
+                attn_stream_t stream);
+
+/* Bytes of workspace attn_decode needs for this shape and split count
+ * (0 when num_splits == 1).  num_splits <= 0 is not resolved here: pass the
+ * value returned by attn_decode_num_splits. */
+size_t attn_decode_workspace_bytes(int B, int Hq, int d, int num_splits);
+
+/* Split count attn_decode uses when given num_splits <= 0: enough CTAs to
+ * cover every SM of the current device about twice, no chunk shorter than
+ * 256 keys, at most 256 splits.  Returns a value >= 1 (or a negative error
+ * code for bad arguments).  Queries the current device's SM count once. */
+int attn_decode_num_splits(int B, int Hq, int Hkv, int max_seqlen);
+
+/* Host-side view of the forward scheduler: unit `unit` of the order maps to
+ * (*b, *h, *m) where m is the index of a 256-row block.  Pure host code; the
+ * same function runs inside the kernel.  Returns ATTN_OK or ATTN_ERR_ARG. */
+int attn_tile_map(int tile_order, int B, int Hq, int N, int causal, long long unit,
+                  int *b, int *h, int *m);
+
+/* Number of work units (B * Hq * ceil(N / 256)) of the forward pass. */
+long long attn_fwd_units(int B, int Hq, int N);
+
+/* Synchronise `stream`, then read and clear the device status word that the
+ * bounded waits set.  Returns ATTN_OK, ATTN_ERR_TIMEOUT or ATTN_ERR_CUDA. */
+int attn_device_status(attn_stream_t stream);
+
+/* Time limit, in nanoseconds, of every device-side barrier wait in later
+ * launches (default 10 s; 0 makes any wait that is not already satisfied run
+ * out at once, which tests use to exercise the timeout path).  Returns the
+ * previous value. */
+long long attn_set_wait_timeout_ns(long long ns);
+
+/* Message for a status code (static storage, never NULL). */
+const char *attn_strerror(int code);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,133 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every
+declared symbol, validates arguments on the host before any CUDA call, and
+its scheduler agrees with the tile-order definitions.  No kernel runs."""
+import os
+import re
+
+import pytest
+
+import attention_fa2_fwd_sm_gb300 as attn
+from attention_fa2_fwd_sm_gb300 import _build
+from oracle import tile_order as T
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+A16 = 0x10000  # a fake 16-byte-aligned address: never dereferenced by these calls
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return attn.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared_functions()
+    assert "attn_fwd" in names and "attn_decode" in names
+    for n in names:
+        assert hasattr(L, n), n
+    assert names == set(attn.SIGNATURES), "binding and header disagree"
+
+
+def test_version_and_messages(L):
+    assert attn.attn_version() >= 100
+    for code in (0, -1, -2, -3, -4, -5):
+        assert attn.strerror(code) and attn.strerror(code) != "unknown status code"
+    assert attn.strerror(-99) == "unknown status code"
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(attn, "_lib", None)
+    monkeypatch.setattr(attn, "LIB_PATH", "/nonexistent/libattn.so")
+    with pytest.raises(RuntimeError):
+        attn.lib()
+
+
+@pytest.mark.parametrize("order", T.ORDERS)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N", [(1, 2, 256), (2, 3, 300), (1, 8, 4096), (3, 5, 1)])
+def test_scheduler_matches_the_definitions(L, order, causal, B, H, N):
+    nb = T.num_blocks(N, 256)
+    assert attn.attn_fwd_units(B, H, N) == B * H * nb
+    for u in range(B * H * nb):
+        assert attn.attn_tile_map(order, B, H, N, causal, u) == T.unit_to_tile(order, u, B, H, nb, causal)
+
+
+def test_scheduler_rejects_bad_units(L):
+    with pytest.raises(attn.AttnError):
+        attn.attn_tile_map(0, 1, 2, 256, False, 2)
+    with pytest.raises(attn.AttnError):
+        attn.attn_tile_map(7, 1, 2, 256, False, 0)
+
+
+def _fwd(**kw):
+    a = dict(q=A16, k=A16, v=A16, o=A16, lse=None, B=1, Hq=2, Hkv=2, N=256, d=64, scale=0.125,
+             causal=False, tile_order=0, stream=0)
+    a.update(kw)
+    return attn.attn_fwd_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"],
+                            a["N"], a["d"], a["scale"], a["causal"], a["tile_order"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_ARG),
+    (dict(o=A16 + 8), attn.ATTN_ERR_ARG),
+    (dict(lse=A16 + 2), attn.ATTN_ERR_ARG),
+    (dict(B=0), attn.ATTN_ERR_ARG),
+    (dict(N=-5), attn.ATTN_ERR_ARG),
+    (dict(Hq=3, Hkv=2), attn.ATTN_ERR_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_ARG),
+    (dict(tile_order=3), attn.ATTN_ERR_ARG),
+    (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+])
+def test_forward_argument_errors(L, kw, code):
+    assert _fwd(**kw) == code
+
+
+def _dec(**kw):
+    a = dict(q=A16, k=A16, v=A16, seqlens=A16, o=A16, B=2, Hq=64, Hkv=8, d=128, scale=0.1,
+             splits=4, s_max=1024, ws=A16, ws_bytes=1 << 30, stream=0)
+    a.update(kw)
+    return attn.attn_decode(a["q"], a["k"], a["v"], a["seqlens"], a["o"], a["B"], a["Hq"], a["Hkv"],
+                            a["d"], a["scale"], a["splits"], a["s_max"], a["ws"], a["ws_bytes"],
+                            a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(seqlens=None), attn.ATTN_ERR_ARG),
+    (dict(k=A16 + 4), attn.ATTN_ERR_ARG),
+    (dict(Hq=60, Hkv=8), attn.ATTN_ERR_ARG),
+    (dict(s_max=0), attn.ATTN_ERR_ARG),
+    (dict(splits=257), attn.ATTN_ERR_ARG),
+    (dict(scale=-1.0), attn.ATTN_ERR_ARG),
+    (dict(d=56), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Hq=64, Hkv=2), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(ws=None), attn.ATTN_ERR_WORKSPACE),
+    (dict(ws_bytes=100), attn.ATTN_ERR_WORKSPACE),
+    (dict(ws=A16 + 8), attn.ATTN_ERR_WORKSPACE),
+])
+def test_decode_argument_errors(L, kw, code):
+    assert _dec(**kw) == code
+
+
+def test_workspace_size(L):
+    assert attn.attn_decode_workspace_bytes(2, 64, 128, 1) == 0
+    n = 2 * 64 * 4
+    o_bytes = -(-(n * 128 * 4) // 256) * 256
+    assert attn.attn_decode_workspace_bytes(2, 64, 128, 4) == o_bytes + n * 4
+
+
+def test_wait_timeout_setting_round_trips(L):
+    old = attn.attn_set_wait_timeout_ns(12345)
+    assert attn.attn_set_wait_timeout_ns(old) == 12345
+
+
+def test_build_is_for_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in _build.ARCH

@@ -1,0 +1,166 @@
+"""GPU parity of the forward kernel against the fp64 oracle, through the C ABI.
+
+Small shapes are compared element by element (several tiles, ragged tails,
+N = 1, GQA, causal, d = 56/64/128); the full sizes of the benchmark
+configurations are compared on sampled rows of sampled heads.  Structural
+identities are checked bit for bit: the three tile orders, GQA against MHA
+with repeated K/V, and d = 56 against explicit zero padding to 64."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic_inputs import prefill_inputs, sample_heads, sample_rows
+from tests.gpu_util import assert_close, scale_of, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def attn():
+    from attention_fa2_fwd_sm_gb300 import _build
+    _build.build()
+    import attention_fa2_fwd_sm_gb300 as A
+    A.lib()
+    oracle.build()
+    return A
+
+
+def _run(A, q, k, v, causal, scale=None, order=0):
+    o, lse = A.forward(q, k, v, causal=causal, scale=scale, tile_order=order)
+    torch.cuda.synchronize()
+    A.check(A.attn_device_status(), "device status")
+    return o, lse
+
+
+SMALL = [
+    # B, Hq, Hkv, N, d, causal
+    (1, 2, 2, 256, 64, False),  # the correctness configuration
+    (1, 2, 2, 256, 64, True),
+    (2, 4, 2, 1, 64, False),
+    (1, 2, 1, 1, 128, True),
+    (1, 2, 2, 100, 128, False),
+    (1, 3, 3, 129, 128, True),
+    (2, 4, 2, 384, 128, True),
+    (1, 8, 1, 700, 128, False),
+    (1, 8, 1, 700, 128, True),
+    (1, 2, 2, 1000, 56, True),
+    (1, 2, 2, 513, 56, False),
+    (2, 2, 2, 300, 64, True),
+    (1, 4, 4, 2048, 128, False),
+    (1, 4, 2, 1537, 64, True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal", SMALL)
+def test_forward_matches_oracle(attn, B, Hq, Hkv, N, d, causal):
+    dev = torch.device("cuda")
+    q, k, v = prefill_inputs(1, B, Hq, Hkv, N, d, dev)
+    scale = scale_of(d)
+    o, lse = _run(attn, q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), scale, causal)
+    assert_close(to64(o), o_ref, to64(lse), lse_ref, what=f"{(B, Hq, Hkv, N, d, causal)}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tile_orders_are_bit_identical_and_correct(attn, causal):
+    """More units than SMs, so persistent CTAs run several units each."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N, d = 1, 64, 8, 2048 + 77, 128
+    q, k, v = prefill_inputs(2, B, Hq, Hkv, N, d, dev)
+    outs = [_run(attn, q, k, v, causal, order=o) for o in (0, 1, 2)]
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+    o, lse = outs[0]
+    scale = scale_of(d)
+    for h in sample_heads(Hq, Hkv):
+        g = h // (Hq // Hkv)
+        rows = sample_rows(N)
+        o_ref, l_ref = oracle.attention_rows(to64(q[0, h, rows]), to64(k[0, g]), to64(v[0, g]), scale,
+                                             causal, rows)
+        assert_close(to64(o[0, h, rows]), o_ref, to64(lse[0, h, rows]), l_ref, what=f"head {h}")
+
+
+def test_d56_equals_zero_padding_to_64(attn):
+    dev = torch.device("cuda")
+    B, H, N = 1, 4, 777
+    q, k, v = prefill_inputs(3, B, H, H, N, 56, dev)
+    scale = scale_of(56)
+    o56, l56 = _run(attn, q, k, v, True, scale)
+    pad = lambda t: torch.nn.functional.pad(t, (0, 8)).contiguous()
+    o64, l64 = _run(attn, pad(q), pad(k), pad(v), True, scale)
+    assert torch.equal(o56, o64[..., :56]) and torch.equal(l56, l64)
+    assert torch.count_nonzero(o64[..., 56:]) == 0
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_equals_mha_with_repeated_kv(attn, causal):
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N, d = 2, 8, 2, 600, 128
+    q, k, v = prefill_inputs(4, B, Hq, Hkv, N, d, dev)
+    o_g, l_g = _run(attn, q, k, v, causal)
+    rep = lambda t: t.repeat_interleave(Hq // Hkv, dim=1).contiguous()
+    o_m, l_m = _run(attn, q, rep(k), rep(v), causal)
+    assert torch.equal(o_g, o_m) and torch.equal(l_g, l_m)
+
+
+def test_repeated_calls_are_deterministic(attn):
+    dev = torch.device("cuda")
+    q, k, v = prefill_inputs(5, 1, 16, 4, 3000, 128, dev)
+    a = _run(attn, q, k, v, True)
+    b = _run(attn, q, k, v, True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_no_lse_and_no_write_past_the_output(attn):
+    """lse may be NULL; the output is written only inside its rows."""
+    dev = torch.device("cuda")
+    B, H, N, d = 1, 2, 300, 64
+    q, k, v = prefill_inputs(6, B, H, H, N, d, dev)
+    out = torch.full((B * H * N * d + 1024,), 7.0, dtype=torch.bfloat16, device=dev)
+    view = out[: B * H * N * d].view(B, H, N, d)
+    attn.check(attn.attn_fwd(q, k, v, view, None, B, H, H, N, d, scale_of(d), False), "attn_fwd")
+    torch.cuda.synchronize()
+    assert torch.all(out[B * H * N * d:] == 7.0)
+    o_ref, _ = oracle.attention(to64(q), to64(k), to64(v), scale_of(d), False)
+    assert_close(to64(view), o_ref, what="no-lse call")
+
+
+FULL = [
+    # name, B, Hq, Hkv, N, d, causal
+    ("mha", 1, 128, 128, 8192, 128, False),
+    ("mha", 1, 128, 128, 32768, 128, False),
+    ("mha", 1, 128, 128, 131072, 128, False),
+    ("gqa", 1, 64, 8, 8192, 128, False),
+    ("gqa", 1, 64, 8, 8192, 128, True),
+    ("gqa", 1, 64, 8, 32768, 128, False),
+    ("gqa", 1, 64, 8, 32768, 128, True),
+    ("gqa", 1, 64, 8, 131072, 128, False),
+    ("gqa", 1, 64, 8, 131072, 128, True),
+    ("deepseek", 1, 128, 128, 32768, 56, True),
+    ("deepseek", 1, 128, 128, 131072, 56, True),
+]
+
+
+@pytest.mark.parametrize("name,B,Hq,Hkv,N,d,causal", FULL)
+def test_full_size_sampled_rows(attn, name, B, Hq, Hkv, N, d, causal):
+    dev = torch.device("cuda")
+    cfg = {"mha": 11, "gqa": 12, "deepseek": 13}[name]
+    q, k, v = prefill_inputs(cfg, B, Hq, Hkv, N, d, dev)
+    scale = scale_of(d)
+    o, lse = _run(attn, q, k, v, causal, scale)
+    rows = sample_rows(N)
+    G = Hq // Hkv
+    try:
+        for h in sample_heads(Hq, Hkv):
+            g = h // G
+            o_ref, l_ref = oracle.attention_rows(to64(q[0, h, rows]), to64(k[0, g]), to64(v[0, g]),
+                                                 scale, causal, rows)
+            assert_close(to64(o[0, h, rows]), o_ref, to64(lse[0, h, rows]), l_ref,
+                         what=f"{name} N={N} causal={causal} head {h}")
+    finally:
+        del q, k, v, o, lse
+        gc.collect()
+        torch.cuda.empty_cache()
