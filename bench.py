@@ -135,7 +135,7 @@ def run_gpu(args):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     scale = 1.0 / math.sqrt(d)
-    Bd, Hq, Hkv, S, dd = DEC["B"], DEC["Hq"], DEC["Hkv"], DEC["S"], DEC["d"]
+    Bd, Hq, Hkv, S, dd = args.dec_batch, DEC["Hq"], DEC["Hkv"], args.dec_len, DEC["d"]
     qd, kc, vc = decode_inputs(70, Bd, Hq, Hkv, S, dd, dev)
     seqlens = torch.full((Bd,), S, dtype=torch.int32, device=dev)
     splits = attn.attn_decode_num_splits(Bd, Hq, Hkv, S)
@@ -374,6 +374,8 @@ def main():
     ap.add_argument("--no-ablation", dest="ablation", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--dec-batch", type=int, default=DEC["B"], help="decode batch")
+    ap.add_argument("--dec-len", type=int, default=DEC["S"], help="decode cached keys per sequence")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=8.0)
     args = ap.parse_args()
