@@ -39,6 +39,7 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
+    "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "attn_tile_map": (_I, [_I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
@@ -115,6 +116,18 @@ def attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, num_splits,
     return lib().attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), B, Hq,
                              Hkv, d, float(scale), int(num_splits), int(max_seqlen),
                              _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def attn_decode_noalloc(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, num_splits, max_seqlen,
+                        stream=None) -> int:
+    """attn_decode for callers that cannot allocate device memory: the split
+    partials go to a scratch array built into the library (see attn.h)."""
+    return lib().attn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), B,
+                                     Hq, Hkv, d, float(scale), int(num_splits), int(max_seqlen),
+                                     _stream(stream))
+
+
+DECODE_NOALLOC_SCRATCH_BYTES = 4194304
 
 
 def attn_decode_workspace_bytes(B, Hq, d, num_splits) -> int:

@@ -227,6 +227,38 @@ int attn_decode(const void *q, const void *kcache, const void *vcache, const int
     return decode_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+static_assert(ATTN_DECODE_NOALLOC_SCRATCH_BYTES == attn::kDecodeNoAllocScratchBytes,
+              "header and library disagree on the built-in scratch size");
+
+int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                        void *o, int B, int Hq, int Hkv, int d, float scale, int num_splits,
+                        int max_seqlen, attn_stream_t stream) {
+    // The argument checks of attn_decode, made here first so that a bad call
+    // is refused before the one-time scratch set-up touches CUDA.
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !seqlens ||
+        (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+        return ATTN_ERR_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || max_seqlen <= 0 || Hq % Hkv) return ATTN_ERR_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_ARG;
+    if (num_splits > kMaxSplits) return ATTN_ERR_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (Hq / Hkv > kDecodeMaxGroup) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || Hkv > 65535 || (long long)max_seqlen * d * 2 >= (1LL << 39)) return ATTN_ERR_ARG;
+    const size_t cap = kDecodeNoAllocScratchBytes;
+    if (num_splits <= 0) {
+        const int sms = current_num_sms();
+        if (sms <= 0) return ATTN_ERR_CUDA;
+        num_splits = splits_for(B, Hkv, max_seqlen, sms);
+        while (num_splits > 1 && attn_decode_workspace_bytes(B, Hq, d, num_splits) > cap) --num_splits;
+    } else if (attn_decode_workspace_bytes(B, Hq, d, num_splits) > cap) {
+        return ATTN_ERR_WORKSPACE;
+    }
+    void *scratch = nullptr;
+    if (decode_noalloc_scratch(&scratch) != cudaSuccess || !scratch) return ATTN_ERR_CUDA;
+    return attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, num_splits, max_seqlen,
+                       scratch, cap, stream);
+}
+
 int attn_device_status(attn_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;

@@ -34,6 +34,13 @@ struct DecodeLaunch {
 int fwd_launch(const FwdLaunch &a, cudaStream_t stream);
 int decode_launch(const DecodeLaunch &a, cudaStream_t stream);
 
+// Size of the built-in scratch array used by attn_decode_noalloc.
+constexpr size_t kDecodeNoAllocScratchBytes = size_t(4) << 20;
+
+// Device address of that array on the current device (looked up on the
+// first call for each device).
+cudaError_t decode_noalloc_scratch(void **ptr);
+
 // Read and clear the status word of each kernel translation unit (OR of
 // kStatus* bits).
 cudaError_t fwd_take_status(int *bits);

@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
@@ -29,6 +30,14 @@
 namespace attn {
 
 static __device__ int g_decode_status;
+
+// Built-in scratch for attn_decode_noalloc: the split partials of callers
+// that cannot hand the library a workspace.  A fixed-size array that is part
+// of the library image, so every GPU that loads the library holds it until
+// the process exits.  Host code must not use the symbol itself as a pointer
+// (on the host it names a stand-in, not device memory); decode_noalloc_scratch
+// looks up the real device address.
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[kDecodeNoAllocScratchBytes];
 
 namespace dec {
 
@@ -400,6 +409,26 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
 int decode_launch(const DecodeLaunch &a, cudaStream_t stream) {
     if (a.d == 64) return dec::launch<64>(a, stream);
     return dec::launch<128>(a, stream);
+}
+
+cudaError_t decode_noalloc_scratch(void **ptr) {
+    // One lookup per device, made with that device current; later calls reuse it.
+    constexpr int kMaxDevices = 64;
+    static void *addr[kMaxDevices] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t decode_take_status(int *bits) {

@@ -121,6 +121,50 @@ int attn_decode(const void *q, const void *kcache, const void *vcache, const int
                 int max_seqlen, void *workspace, size_t workspace_bytes,
                 attn_stream_t stream);
 
+/* Size in bytes of the scratch array built into the library for
+ * attn_decode_noalloc. */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES 4194304u
+
+/*
+ * attn_decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for integration.
+ *
+ * Who needs it: code that may not call cudaMalloc or own a buffer of its
+ * own -- for example a plug-in inside a host framework whose memory pool
+ * has reserved the whole device and forbids side allocations, or a
+ * latency-critical serving loop where an allocation (and the device-wide
+ * synchronisation it can imply) is not acceptable, or a caller whose own
+ * interface has no way to pass a workspace through.  Such a caller still
+ * passes its inputs and its output; the split partials go to a scratch
+ * array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES bytes that is part of the
+ * library image.  Every GPU that loads the library holds that array until
+ * the process exits.  This entry point allocates nothing and calls no
+ * allocating routine.
+ *
+ * Arguments, layouts and results are those of attn_decode, without the
+ * workspace.  num_splits <= 0 takes attn_decode_num_splits' count, lowered
+ * until the partials fit in the scratch (1 split needs none).  An explicit
+ * num_splits whose partials need more than the scratch holds, i.e.
+ * attn_decode_workspace_bytes(B, Hq, d, num_splits) >
+ * ATTN_DECODE_NOALLOC_SCRATCH_BYTES, is refused with ATTN_ERR_WORKSPACE
+ * before any work is queued; argument errors are reported as by
+ * attn_decode.
+ *
+ * Set-up: the first call on each device looks up the device address of the
+ * scratch array (cudaGetSymbolAddress, with that device current) and keeps
+ * it for later calls.  Make that first call before capturing any stream.
+ *
+ * Sharing: all calls use the same array, and it keeps whatever the last call
+ * wrote.  Each call writes every partial it later reads, so nothing needs
+ * clearing between calls.  Calls whose kernels can run at the same time on
+ * the GPU (different streams without ordering between them) race on the
+ * array and give wrong results: order such calls on one stream or with
+ * events.
+ */
+int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache,
+                        const int *seqlens, void *o, int B, int Hq, int Hkv, int d,
+                        float scale, int num_splits, int max_seqlen, attn_stream_t stream);
+
 /* Bytes of workspace attn_decode needs for this shape and split count
  * (0 when num_splits == 1).  num_splits <= 0 is not resolved here: pass the
  * value returned by attn_decode_num_splits. */

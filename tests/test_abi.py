@@ -131,3 +131,14 @@ def test_wait_timeout_setting_round_trips(L):
 
 def test_build_is_for_sm103a():
     assert "arch=compute_103a,code=sm_103a" in _build.ARCH
+
+
+def test_noalloc_decode_refuses_on_the_host(L):
+    """Refusals happen before any CUDA call (no device needed)."""
+    p = (A16, A16, A16, A16, A16)
+    # 32 x 64 heads x 64 splits of 129 floats needs far more than the built-in scratch
+    assert attn.attn_decode_workspace_bytes(32, 64, 128, 64) > attn.DECODE_NOALLOC_SCRATCH_BYTES
+    assert attn.attn_decode_noalloc(*p, 32, 64, 8, 128, 0.1, 64, 4096, 0) == attn.ATTN_ERR_WORKSPACE
+    assert attn.attn_decode_noalloc(None, *p[1:], 2, 64, 8, 128, 0.1, 4, 1024, 0) == attn.ATTN_ERR_ARG
+    assert attn.attn_decode_noalloc(*p, 2, 64, 8, 56, 0.1, 4, 1024, 0) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_decode_noalloc(*p, 2, 64, 8, 128, 0.1, 300, 1024, 0) == attn.ATTN_ERR_ARG
