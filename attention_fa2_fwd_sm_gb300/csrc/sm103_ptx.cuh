@@ -61,12 +61,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of the same condition.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with parity `parity` of barrier `bar` has completed.
 // Gives up after `limit_ns` nanoseconds or as soon as *abort is set by
 // another role of the CTA; on giving up it sets *abort (so the other roles
 // leave too) and ORs kStatusTimeout into *status.  Returns true on success.
+// A limit of 0 fails any wait whose phase is not complete at the first,
+// non-blocking probe.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                   volatile int *abort, int *status) {
+    if (limit_ns == 0) {
+        if (mbar_test_wait(bar, parity)) return true;
+        *abort = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -87,6 +108,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 // that follow never see a partial warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                volatile int *abort, int *status) {
+    if (limit_ns == 0) {
+        if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+        if ((threadIdx.x & 31) == 0) {
+            *abort = 1;
+            atomicOr(status, kStatusTimeout);
+        }
+        __syncwarp();
+        return false;
+    }
     bool done = mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
     const uint64_t t0 = global_timer_ns();

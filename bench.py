@@ -306,7 +306,7 @@ def cpu_baseline(q, k, v, scale, causal, budget_s):
     """The fp64 oracle as it stands, on rows of head 0 of the same workload."""
     import numpy as np
     N = q.shape[2]
-    rows = min(N, 8192)
+    rows = N
     positions = np.arange(rows, dtype=np.int64)
     qh = q[0, 0, :rows].double().cpu().numpy()
     kh = k[0, 0].double().cpu().numpy()
