@@ -47,6 +47,7 @@ SIGNATURES = {
     "attn_device_status": (_I, [_P]),
     "attn_set_wait_timeout_ns": (_LL, [_LL]),
     "attn_strerror": (ctypes.c_char_p, [_I]),
+    "attn_last_error": (ctypes.c_char_p, []),
     "attn_version": (_I, []),
 }
 
@@ -56,7 +57,10 @@ _lib = None
 class AttnError(RuntimeError):
     def __init__(self, code: int, what: str = ""):
         self.code = code
-        super().__init__(f"{what}: {strerror(code)} ({code})" if what else f"{strerror(code)} ({code})")
+        msg = f"{what}: {strerror(code)} ({code})" if what else f"{strerror(code)} ({code})"
+        if code == ATTN_ERR_CUDA:
+            msg += f" [{attn_last_error()}]"
+        super().__init__(msg)
 
 
 def lib():
@@ -156,6 +160,10 @@ def attn_device_status(stream=None) -> int:
 
 def attn_set_wait_timeout_ns(ns: int) -> int:
     return int(lib().attn_set_wait_timeout_ns(int(ns)))
+
+
+def attn_last_error() -> str:
+    return lib().attn_last_error().decode()
 
 
 def attn_version() -> int:

@@ -8,6 +8,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <mutex>
 
 #include "../../include/attn.h"
@@ -58,6 +59,15 @@ constexpr int kDecodeMaxGroup = 16;
 
 }  // namespace
 
+namespace {
+thread_local char g_last_error[256] = "";
+}
+
+int note_cuda_error(cudaError_t e, const char *where) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), int(e));
+    return ATTN_ERR_CUDA;
+}
+
 bool encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
                     uint32_t box0, uint32_t box1) {
     EncodeTiledFn fn = encode_fn();
@@ -78,6 +88,8 @@ using namespace attn;
 extern "C" {
 
 int attn_version(void) { return 100; }
+
+const char *attn_last_error(void) { return g_last_error; }
 
 const char *attn_strerror(int code) {
     switch (code) {
@@ -134,7 +146,7 @@ int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
     int rc = validate_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, tile_order);
     if (rc != ATTN_OK) return rc;
     const int sms = current_num_sms();
-    if (sms <= 0) return ATTN_ERR_CUDA;
+    if (sms <= 0) return note_cuda_error(cudaErrorNoDevice, "device query");
     FwdLaunch a;
     a.q = q;
     a.k = k;
@@ -168,10 +180,17 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int d, int num_splits) {
     return o_bytes + parts * sizeof(float);
 }
 
+// Split count: aim at about 5/3 CTAs per SM in all (the decode kernel keeps
+// two CTAs resident per SM, and a grid just over one wave leaves a tail wave
+// on a few SMs), never below 512 keys per split, at most kMaxSplits.  Chosen
+// from a sweep of split counts over batch {1, 8, 32} x keys {8K, 32K, 128K}
+// (H_Q = 64, H_KV = 8, d = 128), where it lands within a few percent of the
+// best split count in every configuration.
 static int splits_for(int B, int Hkv, int max_seqlen, int sms) {
     const long long ctas = (long long)B * Hkv;
-    long long s = (2LL * sms + ctas - 1) / ctas;
-    const long long by_len = (max_seqlen + 255) / 256;
+    const long long target = (5LL * sms) / 3;
+    long long s = (target + ctas / 2) / ctas;  // round to nearest
+    const long long by_len = max_seqlen / 512;
     if (s > by_len) s = by_len;
     if (s > kMaxSplits) s = kMaxSplits;
     if (s < 1) s = 1;
@@ -254,7 +273,8 @@ int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, c
         return ATTN_ERR_WORKSPACE;
     }
     void *scratch = nullptr;
-    if (decode_noalloc_scratch(&scratch) != cudaSuccess || !scratch) return ATTN_ERR_CUDA;
+    const cudaError_t se = decode_noalloc_scratch(&scratch);
+    if (se != cudaSuccess || !scratch) return note_cuda_error(se, "cudaGetSymbolAddress(scratch)");
     return attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, num_splits, max_seqlen,
                        scratch, cap, stream);
 }

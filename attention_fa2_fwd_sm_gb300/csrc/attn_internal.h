@@ -30,6 +30,10 @@ struct DecodeLaunch {
     unsigned long long wait_ns;
 };
 
+// Record a failed CUDA call for attn_last_error() (this thread) and return
+// ATTN_ERR_CUDA.
+int note_cuda_error(cudaError_t e, const char *where);
+
 // Each returns 0 or a negative ATTN_ERR_* code.
 int fwd_launch(const FwdLaunch &a, cudaStream_t stream);
 int decode_launch(const DecodeLaunch &a, cudaStream_t stream);

@@ -374,7 +374,7 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
                         kKeysPerStage) ||
         !encode_bf16_3d(&mv, a.vcache, D, uint64_t(a.max_seqlen), uint64_t(a.B) * a.Hkv, 64,
                         kKeysPerStage))
-        return -4;
+        return note_cuda_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled (decode)");
     Params p;
     p.q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
     p.seqlens = a.seqlens;
@@ -390,16 +390,18 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
     p.wait_ns = a.wait_ns;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes) != cudaSuccess)
-            return -4;
+        const cudaError_t e = cudaFuncSetAttribute(
+            decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(decode_kernel)");
         attr_set = true;
     }
     decode_kernel<D><<<dim3(a.num_splits, a.Hkv, a.B), dim3(kThreads), C::kSmemBytes, stream>>>(mk, mv, p);
-    if (cudaGetLastError() != cudaSuccess) return -4;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return note_cuda_error(e, "decode_kernel launch");
     if (a.num_splits > 1) {
         merge_kernel<D><<<dim3(a.B * a.Hq), dim3(D), 0, stream>>>(a.ws_o, a.ws_lse, p.o, a.num_splits);
-        if (cudaGetLastError() != cudaSuccess) return -4;
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return note_cuda_error(e, "merge_kernel launch");
     }
     return 0;
 }

@@ -8,11 +8,16 @@
 // "Fused Grouped-Query Attention", short-context section: running
 // accumulators (m, l, O)).
 //
-// Design (one persistent CTA per SM, 12 warps):
+// Design (one persistent CTA per SM, 12 warps = 3 warpgroups):
 //   warp 0      TMA producer: Q tiles, then a ring of K/V blocks (128 keys).
 //   warp 1      tcgen05 issuer (one thread) + TMEM owner.
+//   warps 2-3   idle (they complete the control warpgroup).
 //   warps 4-7   softmax / epilogue of MMA tile 0 (query rows 0-127 of the unit)
 //   warps 8-11  softmax / epilogue of MMA tile 1 (rows 128-255)
+// A warp may only touch TMEM lanes [32 (w % 4), +32), so each warpgroup
+// covers the 128 rows of its tile once.  After set-up the control warpgroup
+// gives registers back (setmaxnreg) so each softmax thread can hold a whole
+// 128-column row of S in registers.
 // A unit is 256 query rows of one head: two 128-row MMA tiles share every
 // K/V block loaded into shared memory.  TMEM (512 columns): S/P of tile t at
 // columns [128 t, 128 t + 128), O of tile t at [256 + D t, 256 + D t + D).
@@ -42,6 +47,14 @@ constexpr int kTileM = 128;    // query rows per MMA tile
 constexpr int kBlockN = 128;   // keys per K/V block
 constexpr int kNT = 2;         // MMA tiles per unit
 constexpr int kThreads = 384;  // 12 warps
+// Register split after set-up.  The launch gives 168 registers per thread
+// (65536 / 384, rounded down to a multiple of 8): 384 x 168 = 64512 in all.
+// The split must not exceed that or setmaxnreg.inc would wait forever; the
+// host checks the compiled count before every launch.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 120;
+constexpr int kSoftmaxRegs = 184;
+static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (log2 units)
 
@@ -161,7 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long u_step = persistent ? (long long)gridDim.x : p.total_units;
     int *status = &g_fwd_status;
 
-    if (warp == 0) {
+    // Each role runs inside the branch that set its register limit, so the
+    // compiler allocates each role's code under that role's limit.
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+      if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             long long fills = 0;          // K/V ring fills issued
@@ -237,25 +254,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return mbar_wait_bounded(bar(C::kBarKVFull + int(f % C::kStages)),
                                          uint32_t((f / C::kStages) & 1), p.wait_ns, abort_flag, status);
             };
-            auto slot_addr = [&](long long f) {
-                return smem_u32(sKV + int(f % C::kStages) * C::kKVBytes);
+            // Descriptors of the first Q tile and the first ring slot; every other
+            // operand start is base + (byte offset >> 4) in the 14-bit address
+            // field (shared-memory offsets stay below 256 KiB, so no carry).
+            const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dK = smem_desc_sw128(smem_u32(sKV), 16, 1024);
+            const uint64_t dV = smem_desc_sw128(smem_u32(sKV), C::kChunkBytes, 1024);
+            auto slot_off = [&](long long f) {
+                return uint64_t(int(f % C::kStages) * (C::kKVBytes >> 4));
             };
             auto issue_qk = [&](int t, long long fK) {
-                const uint32_t qa = smem_u32(sQ + t * C::kQBytes);
-                const uint32_t ka = slot_addr(fK);
+                const uint64_t a0 = dQ + uint64_t(t * (C::kQBytes >> 4));
+                const uint64_t b0 = dK + slot_off(fK);
+                const uint32_t d_tmem = tmem_base + t * kTileM;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                    tc_mma_ss(tmem_base + t * kTileM, smem_desc_sw128(qa + off, 16, 1024),
-                              smem_desc_sw128(ka + off, 16, 1024), kIdescQK, kk > 0);
+                    const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
+                    tc_mma_ss(d_tmem, a0 + off, b0 + off, kIdescQK, kk > 0);
                 }
             };
             auto issue_pv = [&](int t, long long fV, bool acc) {
-                const uint32_t va = slot_addr(fV);
+                const uint64_t b0 = dV + slot_off(fV);
+                const uint32_t d_tmem = tmem_base + C::kOCol + t * D;
+                const uint32_t a_tmem = tmem_base + t * kTileM;
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    tc_mma_ts(tmem_base + C::kOCol + t * D, tmem_base + t * kTileM + kk * 8,
-                              smem_desc_sw128(va + kk * 16 * 128, C::kChunkBytes, 1024), kIdescPV,
+                    tc_mma_ts(d_tmem, a_tmem + kk * 8, b0 + uint64_t((kk * 16 * 128) >> 4), kIdescPV,
                               (acc || kk > 0) ? 1u : 0u);
                 }
             };
@@ -324,7 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(status, kStatusDrainTimeout);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         // ------------------------------------------------- softmax / epilogue
         const int t = (warp - 4) >> 2;      // MMA tile of this warpgroup
         const int quarter = warp & 3;       // TMEM lane quarter of this warp
@@ -369,9 +395,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 128; ++c)
                         if (c >= lim) s[c] = -INFINITY;
                 }
-                float mx = s[0];
+                // Row maximum: four independent chains of three-input maxima.
+                float mq[4];
 #pragma unroll
-                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+                for (int c = 0; c < 4; ++c) {
+                    float m = fmax3(s[32 * c], s[32 * c + 1], s[32 * c + 2]);
+#pragma unroll
+                    for (int i = 3; i < 31; i += 2) m = fmax3(m, s[32 * c + i], s[32 * c + i + 1]);
+                    mq[c] = fmaxf(m, s[32 * c + 31]);
+                }
+                const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
                 const float m_new = fmaxf(m_run, mx * sl2);
                 float corr = 1.f;
                 if (m_new > m_run + kRescaleLog2) {
@@ -381,19 +414,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l_run *= corr;
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
 
-                // P = 2^(s*scale*log2e - m) in bf16, written over S in TMEM.
+                // P = 2^(s*scale*log2e - m) in bf16, written over S in TMEM; the
+                // row sum goes to four independent pairs of partial sums.
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = fast_exp2(fmaf(s[c * 32 + 2 * i], sl2, neg_m));
-                        const float p1 = fast_exp2(fmaf(s[c * 32 + 2 * i + 1], sl2, neg_m));
-                        l_run += p0 + p1;
+                        float x0, x1;
+                        ffma2(x0, x1, s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1], sl2, sl2, neg_m, neg_m);
+                        const float p0 = fast_exp2(x0);
+                        const float p1 = fast_exp2(x1);
+                        const int a = (i & 3) * 2;
+                        fadd2(ls[a], ls[a + 1], p0, p1);
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     tmem_st16(tS + c * 16, pk);
                 }
+                l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 // Rescale this row of O when its reference maximum moved (never on
                 // the first block: PV(t, 0) overwrites O).
                 if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
@@ -464,7 +503,7 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
     if (!encode_bf16_3d(&mq, a.q, dq, uint64_t(a.N), uint64_t(a.B) * a.Hq, 64, kTileM) ||
         !encode_bf16_3d(&mk, a.k, dq, uint64_t(a.N), uint64_t(a.B) * a.Hkv, 64, kBlockN) ||
         !encode_bf16_3d(&mv, a.v, dq, uint64_t(a.N), uint64_t(a.B) * a.Hkv, 64, kBlockN))
-        return -4;
+        return note_cuda_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled (forward)");
     Params p;
     p.o = reinterpret_cast<__nv_bfloat16 *>(a.o);
     p.lse = a.lse;
@@ -481,16 +520,25 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
     p.wait_ns = a.wait_ns;
     static bool attr_set = false;  // per instantiation; the attribute is per function
     if (!attr_set) {
-        if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes) != cudaSuccess)
-            return -4;
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_kernel<D>);
+        if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncGetAttributes(fwd_kernel)");
+        // The setmaxnreg split assumes the launch register count; refuse to
+        // launch a build that differs (its setmaxnreg.inc could never finish).
+        if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
+            return note_cuda_error(cudaErrorInvalidConfiguration,
+                                   "fwd_kernel register count differs from the setmaxnreg split");
+        e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::kSmemBytes);
+        if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(fwd_kernel)");
         attr_set = true;
     }
     long long grid = p.total_units;
     if (a.order != kNaiveHeadFirst && grid > a.num_sms) grid = a.num_sms;
     if (grid > 0x7fffffffLL) return -2;
     fwd_kernel<D><<<dim3(unsigned(grid)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? 0 : note_cuda_error(e, "fwd_kernel launch");
 }
 
 }  // namespace fwd

@@ -105,6 +105,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats over all ranks of the default
+    process group (the values unchanged when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_throughput(work_per_rank, world, seconds):
+    """Whole-job throughput of `world` independent replicas that each did
+    `work_per_rank` in at most `seconds` (the slowest rank's time)."""
+    return world * work_per_rank / seconds
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -185,17 +203,11 @@ def run_gpu(args):
     fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
 
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, sum(fwd_ms), sum(dec_ms)], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, fwd_sum, dec_sum = t.tolist()
-    else:
-        fwd_sum, dec_sum = sum(fwd_ms), sum(dec_ms)
+    total_ms, fwd_sum, dec_sum = max_over_ranks([total_ms, sum(fwd_ms), sum(dec_ms)], dev)
 
     flops = fwd_flops(B, H, N, d, causal)
     fwd_avg_s = fwd_sum / K / 1e3
-    value = ws * flops / fwd_avg_s / 1e12
+    value = replica_throughput(flops, ws, fwd_avg_s) / 1e12
     peaks, peak_src = load_peaks()
     per_gpu = flops / fwd_avg_s / 1e12
     dec_bytes = 2 * Bd * Hkv * S * dd * 2 + 2 * Bd * Hq * dd * 2
@@ -362,12 +374,126 @@ def run_reference(args):
     }
 
 
+def _l2_flush_buffer(torch, dev):
+    """A buffer twice the L2 size; writing it evicts the previous call's data."""
+    props = torch.cuda.get_device_properties(dev)
+    return torch.empty(2 * max(props.L2_cache_size, 128 << 20), dtype=torch.uint8, device=dev)
+
+
+def _time_calls(torch, fn, reps, flush=None, stream=None):
+    """Median CUDA-event time (ms) of ``fn`` over ``reps`` calls, each after an
+    optional L2 flush outside the events."""
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
+
+
+def run_decode_sweep(args):
+    """Decode configurations (H_Q=64, H_KV=8, d=128; batch x KV length) with
+    num_splits swept; one JSON line per configuration."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import decode_inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    flush = _l2_flush_buffer(torch, dev)
+    stream = torch.cuda.current_stream(dev)
+    Hq, Hkv, d = DEC["Hq"], DEC["Hkv"], DEC["d"]
+    for B in (1, 8, 32):
+        for S in (8192, 32768, 131072):
+            q, kc, vc = decode_inputs(70, B, Hq, Hkv, S, d, dev)
+            seqlens = torch.full((B,), S, dtype=torch.int32, device=dev)
+            o = torch.empty_like(q)
+            nbytes = 2 * B * Hkv * S * d * 2 + 2 * B * Hq * d * 2
+            heur = attn.attn_decode_num_splits(B, Hq, Hkv, S)
+            cands = sorted({1, 2, 3, 4, 5, 6, 8, 12, 16, 19, 24, 32, 38, 48, 64, heur})
+            res = {}
+            for sp in cands:
+                if sp > 1 and -(-S // sp) < 64:
+                    continue
+                wb = attn.attn_decode_workspace_bytes(B, Hq, d, sp)
+                ws = torch.empty(max(wb, 16), dtype=torch.uint8, device=dev)
+                fn = lambda: attn.check(attn.attn_decode(q, kc, vc, seqlens, o, B, Hq, Hkv, d, d ** -0.5,
+                                                         sp, S, ws, wb, stream.cuda_stream), "decode")
+                for _ in range(3):
+                    fn()
+                ms = _time_calls(torch, fn, args.steps, flush, stream)
+                res[sp] = {"us": round(ms * 1e3, 2), "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+            best = max(res, key=lambda k: res[k]["gbs"])
+            print(json.dumps({"mode": "decode-sweep", "B": B, "S": S, "bytes": nbytes,
+                              "heuristic_splits": heur, "heuristic": res.get(heur),
+                              "best_splits": best, "best": res[best],
+                              "frac_hbm_best": round(res[best]["gbs"] / peaks["hbm_gbs"], 4),
+                              "splits": res, "l2": "flushed before every call"}), flush=True)
+            del q, kc, vc
+            torch.cuda.empty_cache()
+
+
+def run_fwd_sweep(args):
+    """Forward configurations of the pages' sweeps, each with the three tile
+    orders; one JSON line per configuration."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import prefill_inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    configs = []
+    for N in (8192, 32768, 131072):
+        configs.append(("mha", 1, 128, 128, N, 128, False))
+    for N in (8192, 32768, 131072):
+        for causal in (False, True):
+            configs.append(("gqa", 1, 64, 8, N, 128, causal))
+    for N in (32768, 131072):
+        configs.append(("deepseek", 1, 128, 128, N, 56, True))
+    for name, B, Hq, Hkv, N, d, causal in configs:
+        q, k, v = prefill_inputs(11, B, Hq, Hkv, N, d, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+        flops = fwd_flops(B, Hq, N, d, causal)
+        out = {"mode": "fwd-sweep", "config": name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
+               "causal": causal, "flops": flops}
+        reps = 3 if N >= 131072 else args.steps
+        for oname, oid in attn.ORDERS.items():
+            fn = lambda: attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, d ** -0.5, causal,
+                                                     oid, stream.cuda_stream), "fwd")
+            fn()
+            ms = _time_calls(torch, fn, reps, None, stream)
+            tf = flops / (ms / 1e3) / 1e12
+            out[oname] = {"ms": round(ms, 3), "tflops": round(tf, 1),
+                          "frac": round(tf / peaks["bf16_tflops"], 4)}
+            if d == 56:
+                out[oname]["tflops_padded_d64"] = round(tf * 64 / 56, 1)
+        print(json.dumps(out), flush=True)
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--mode", default="step", choices=["step", "decode-sweep", "fwd-sweep"],
+                    help="step: the contract's one-line benchmark; the sweeps print one line "
+                         "per configuration")
     ap.add_argument("--n", type=int, default=FWD["N"], help="forward sequence length")
     ap.add_argument("--order", default="head_first", choices=["head_first", "block_first",
                                                               "naive_head_first"])
@@ -380,6 +506,10 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=8.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.mode == "decode-sweep":
+        return run_decode_sweep(args)
+    if args.mode == "fwd-sweep":
+        return run_fwd_sweep(args)
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)

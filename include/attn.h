@@ -170,10 +170,10 @@ int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache,
  * value returned by attn_decode_num_splits. */
 size_t attn_decode_workspace_bytes(int B, int Hq, int d, int num_splits);
 
-/* Split count attn_decode uses when given num_splits <= 0: enough CTAs to
- * cover every SM of the current device about twice, no chunk shorter than
- * 256 keys, at most 256 splits.  Returns a value >= 1 (or a negative error
- * code for bad arguments).  Queries the current device's SM count once. */
+/* Split count attn_decode uses when given num_splits <= 0: about 5/3 CTAs
+ * per SM of the current device in all (B * Hkv * splits), no split shorter
+ * than 512 keys, at most 256 splits.  Returns a value >= 1 (or a negative
+ * error code for bad arguments).  Queries the current device's SM count once. */
 int attn_decode_num_splits(int B, int Hq, int Hkv, int max_seqlen);
 
 /* Host-side view of the forward scheduler: unit `unit` of the order maps to
@@ -194,6 +194,11 @@ int attn_device_status(attn_stream_t stream);
  * out at once, which tests use to exercise the timeout path).  Returns the
  * previous value. */
 long long attn_set_wait_timeout_ns(long long ns);
+
+/* Description of the last failed CUDA call made by this library on the
+ * calling thread (the call behind the last ATTN_ERR_CUDA), or "" if none.
+ * Thread-local storage; valid until the next failing call on this thread. */
+const char *attn_last_error(void);
 
 /* Message for a status code (static storage, never NULL). */
 const char *attn_strerror(int code);
