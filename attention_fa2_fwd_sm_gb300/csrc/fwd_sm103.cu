@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "attn_internal.h"
@@ -40,6 +41,14 @@
 namespace attn {
 
 static __device__ int g_fwd_status;
+
+// Work counters of the persistent forward kernel: for each of kSchedSlots
+// launch slots, {next unit to hand out, CTAs finished}.  CTAs take units in
+// the chosen order by atomically incrementing `next`; the last CTA of the
+// launch to finish resets both to zero.  Successive launches rotate over the
+// slots, so launches only share a slot kSchedSlots launches apart.
+constexpr int kSchedSlots = 64;
+static __device__ unsigned int g_fwd_work[kSchedSlots][2];
 
 namespace fwd {
 
@@ -52,8 +61,8 @@ constexpr int kThreads = 384;  // 12 warps
 // The split must not exceed that or setmaxnreg.inc would wait forever; the
 // host checks the compiled count before every launch.
 constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 120;
-constexpr int kSoftmaxRegs = 184;
+constexpr int kCtrlRegs = 104;
+constexpr int kSoftmaxRegs = 192;
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (log2 units)
@@ -71,9 +80,11 @@ struct Cfg {
     static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarSFull = 4, kBarPFull = 6,
                          kBarOFull = 8, kBarOEmpty = 10, kBarKVFull = 12,
                          kBarKVEmpty = 12 + kStages, kBarDrain = 12 + 2 * kStages,
-                         kNumBars = 13 + 2 * kStages;
+                         kBarUQFull = 13 + 2 * kStages, kBarUQEmpty = 15 + 2 * kStages,
+                         kNumBars = 17 + 2 * kStages;
     static constexpr int kDataBytes = kNT * kQBytes + kStages * kKVBytes;
-    static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 16 + 1024;  // + align slack
+    // data, barriers, TMEM address, abort flag, two-entry unit queue, align slack
+    static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 32 + 1024;
 };
 
 struct Params {
@@ -83,6 +94,7 @@ struct Params {
     long long total_units;
     float scale_log2;
     unsigned long long wait_ns;
+    int sched_slot;  // g_fwd_work slot of this launch (persistent orders)
 };
 
 struct UnitWork {
@@ -112,6 +124,17 @@ __device__ __forceinline__ UnitWork unit_work(const Params &p, long long u) {
     return w;
 }
 
+// The i-th unit this CTA processes, or -1 when there is none left.  Naive
+// head-first: one unit per CTA, its block index.  Otherwise the next unit of
+// the order from the launch's work counter, so CTAs running at the same time
+// hold consecutive units (one ACC at a time in head-first order) and faster
+// CTAs simply take more units.
+__device__ __forceinline__ long long fetch_unit(const Params &p, long long i) {
+    if (p.order == kNaiveHeadFirst) return i == 0 ? (long long)blockIdx.x : -1;
+    const unsigned int u = atomicAdd(&g_fwd_work[p.sched_slot][0], 1u);
+    return (long long)u < p.total_units ? (long long)u : -1;
+}
+
 // Last tile (highest index) that still uses K/V block j.
 __device__ __forceinline__ int last_user(const UnitWork &w, int j) {
     int last = -1;
@@ -134,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kDataBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *unit_q = reinterpret_cast<volatile int *>(tmem_slot + 2);  // 2 entries
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -144,15 +168,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::kBarQFull + t), 1);
             mbar_init(bar(C::kBarQEmpty + t), 1);
             mbar_init(bar(C::kBarSFull + t), 1);
-            mbar_init(bar(C::kBarPFull + t), kTileM);
+            mbar_init(bar(C::kBarPFull + t), 4);   // one arrival per softmax warp
             mbar_init(bar(C::kBarOFull + t), 1);
-            mbar_init(bar(C::kBarOEmpty + t), kTileM);
+            mbar_init(bar(C::kBarOEmpty + t), 4);
         }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(C::kBarKVFull + s), 1);
             mbar_init(bar(C::kBarKVEmpty + s), 1);
         }
         mbar_init(bar(C::kBarDrain), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::kBarUQFull + i), 1);
+            mbar_init(bar(C::kBarUQEmpty + i), 1 + 8);  // MMA thread + 8 softmax warps
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -170,8 +198,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const bool persistent = p.order != kNaiveHeadFirst;
-    const long long u_step = persistent ? (long long)gridDim.x : p.total_units;
     int *status = &g_fwd_status;
 
     // Each role runs inside the branch that set its register limit, so the
@@ -184,7 +210,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long fills = 0;          // K/V ring fills issued
             int q_loads[kNT] = {0, 0};    // Q loads issued per tile
             bool ok = true;
-            for (long long u = blockIdx.x; ok && u < p.total_units; u += u_step) {
+            for (long long qi = 0; ok; ++qi) {
+                // Publish the next unit to the other roles (two-entry queue).
+                const long long u = fetch_unit(p, qi);
+                const int qs = int(qi & 1);
+                if (qi >= 2 && !mbar_wait_bounded(bar(C::kBarUQEmpty + qs), uint32_t(((qi >> 1) - 1) & 1),
+                                                  p.wait_ns, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                unit_q[qs] = int(u);
+                mbar_arrive(bar(C::kBarUQFull + qs));
+                if (u < 0) break;
                 const UnitWork w = unit_work(p, u);
                 for (int t = 0; t < kNT && ok; ++t) {
                     if (w.nkv[t] == 0) continue;
@@ -284,7 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
 
-            for (long long u = blockIdx.x; ok && u < p.total_units; u += u_step) {
+            for (long long qi = 0; ok; ++qi) {
+                const int qs = int(qi & 1);
+                ok = mbar_wait_bounded(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns,
+                                       abort_flag, status);
+                if (!ok) break;
+                const long long u = unit_q[qs];
+                mbar_arrive(bar(C::kBarUQEmpty + qs));
+                if (u < 0) break;
                 const UnitWork w = unit_work(p, u);
                 const long long f0 = fills;  // K_j at f0 + 2j, V_j at f0 + 2j + 1
                 // prologue: S(t, 0) = Q(t) K_0^T
@@ -362,7 +406,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         int s_waits = 0, o_waits = 0;
         bool ok = true;
 
-        for (long long u = blockIdx.x; ok && u < p.total_units; u += u_step) {
+        for (long long qi = 0; ok; ++qi) {
+            const int qs = int(qi & 1);
+            ok = mbar_wait_warp(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag,
+                                status);
+            if (!ok) break;
+            const long long u = unit_q[qs];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarUQEmpty + qs));
+            if (u < 0) break;
             const UnitWork w = unit_work(p, u);
             const int nkv = w.nkv[t];
             if (nkv == 0) continue;
@@ -448,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(C::kBarPFull + t));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarPFull + t));
             }
             if (!ok) break;
 
@@ -483,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok && p.lse)
                 p.lse[(size_t)(w.b * p.Hq + w.h) * p.N + row] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
             tc_fence_before();
-            mbar_arrive(bar(C::kBarOEmpty + t));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarOEmpty + t));
         }
     }
 
@@ -492,6 +546,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
+    }
+    if (threadIdx.x == 0 && p.order != kNaiveHeadFirst) {
+        // Every CTA has fetched its last unit before it gets here, so the last
+        // CTA to arrive may reset the launch's counters for the next user.
+        __threadfence();
+        const unsigned int done = atomicAdd(&g_fwd_work[p.sched_slot][1], 1u);
+        if (done == gridDim.x - 1) {
+            atomicExch(&g_fwd_work[p.sched_slot][0], 0u);
+            atomicExch(&g_fwd_work[p.sched_slot][1], 0u);
+        }
     }
 }
 
@@ -518,6 +582,8 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
     p.total_units = (long long)a.B * a.Hq * p.nb;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_ns = a.wait_ns;
+    static std::atomic<unsigned int> launch_seq{0};
+    p.sched_slot = int(launch_seq.fetch_add(1) % kSchedSlots);
     static bool attr_set = false;  // per instantiation; the attribute is per function
     if (!attr_set) {
         cudaFuncAttributes fa;
