@@ -34,6 +34,35 @@ FWD = dict(B=1, H=128, N=32768, d=128, causal=False)
 DEC = dict(B=8, Hq=64, Hkv=8, S=32768, d=128)
 
 
+# DRAM bytes (read + write) per launch measured with ncu for the kernels as
+# they stand in the listed sources (profiles/ holds the summaries and the
+# commands).  A value is reported only while the sources hash to the same
+# digest; after any change to them the bench reports null until re-captured.
+MEASURED_TRAFFIC = {
+    "fwd": {"files": ["fwd_sm103.cu", "sm103_ptx.cuh", "tile_order.cuh"],
+            "sha256": "785a92a3b768b25cd7cc352788736fba578bcbaa5406a020acf185958fbc329f",
+            # MHA B=1 H=128 d=128, head-first, captured at N=32768 and N=8192
+            "bytes_by_n": {32768: 3234283776 + 1089613056, 8192: 806984448 + 252358912}},
+    "decode": {"files": ["decode_sm103.cu", "sm103_ptx.cuh"],
+               "sha256": "41e8476af5f5dbf468fb89d766525d8bc21502a58da309f748346aaa6c9f9e33",
+               # GQA decode B=8 Hq=64 Hkv=8 d=128, 4 splits, captured at 8192 keys;
+               # the bytes scale with the keys streamed
+               "bytes_per_key": (268595456 + 4392448) / 8192.0, "batch": 8},
+}
+
+
+def measured_traffic(kind):
+    """The ncu-measured traffic entry for `kind` if the kernel sources are
+    unchanged since the capture, else None."""
+    import hashlib
+    entry = MEASURED_TRAFFIC[kind]
+    h = hashlib.sha256()
+    for f in entry["files"]:
+        with open(os.path.join(ROOT, "attention_fa2_fwd_sm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return entry if h.hexdigest() == entry["sha256"] else None
+
+
 def fwd_flops(B, H, N, d, causal):
     f = 4.0 * B * H * N * N * d
     return f / 2 if causal else f
@@ -214,6 +243,11 @@ def run_gpu(args):
     dec_avg_s = dec_sum / K / 1e3
     dec_gbs = dec_bytes / dec_avg_s / 1e9
 
+    tf = measured_traffic("fwd")
+    fwd_traffic = (tf["bytes_by_n"].get(N) if (tf and B == 1 and H == 128 and d == 128 and not causal
+                                              and args.order == "head_first") else None)
+    td = measured_traffic("decode")
+    dec_traffic = (round(td["bytes_per_key"] * S * Bd / td["batch"]) if (td and splits == 4) else None)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 3), "higher_is_better": True,
@@ -226,11 +260,11 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (no flush)"},
         "roofline": {"bound": "tensor", "achieved": round(per_gpu, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(per_gpu / peaks["bf16_tflops"], 4), "traffic": None,
+                     "frac": round(per_gpu / peaks["bf16_tflops"], 4), "traffic": fwd_traffic,
                      "peak_source": f"{peak_src} bf16 burst", "kernel": "fwd_kernel<128>"},
         "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "us_per_step": round(dec_avg_s * 1e6, 2),
                    "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4), "hbm_peak_gbs": peaks["hbm_gbs"],
-                   "bytes_per_step": dec_bytes},
+                   "bytes_per_step": dec_bytes, "traffic": dec_traffic},
         "gpu_launches": K * (1 + (2 if splits > 1 else 1)),
         "clocks": clk.summary(),
     }
