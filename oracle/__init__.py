@@ -6,7 +6,8 @@ library and its Python binding) never imports, links or runs anything here,
 and this package imports nothing from the product.
 
 The arithmetic lives in ``attn_oracle.c`` (the plain definition of attention,
-row by row, in double precision, and the log-sum-exp merge); this module only
+row by row, in double precision, its gradient by the chain rule, and the
+log-sum-exp merge); this module only
 builds it with gcc, marshals numpy arrays and applies the readings that the
 pages leave open:
 
@@ -64,6 +65,10 @@ def _load():
         lib.oracle_attention_head.restype = ctypes.c_int
         lib.oracle_lse_merge.argtypes = [_D, _D, ctypes.c_int64, ctypes.c_int64, _D, _D]
         lib.oracle_lse_merge.restype = ctypes.c_int
+        lib.oracle_attention_bwd_head.argtypes = [
+            _D, _D, _D, _D, _I64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_double, ctypes.c_int, _D, _D, _D, ctypes.c_int]
+        lib.oracle_attention_bwd_head.restype = ctypes.c_int
         lib.oracle_default_threads.argtypes = []
         lib.oracle_default_threads.restype = ctypes.c_int
         _lib = lib
@@ -109,6 +114,29 @@ def attention_head(q, k, v, scale, causal=False, qpos=None, k_lo=0, k_hi=None, n
     return o, lse
 
 
+def attention_bwd_head(q, k, v, dout, scale, causal=False, qpos=None, nthreads=0):
+    """Gradients of one head for output gradient ``dout [nq, d]``:
+    ``(dq [nq, d], dk [nk, d], dv [nk, d])`` in fp64 (chain rule of the
+    forward definition; see ``attn_oracle.c``)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    nq, d = q.shape
+    nk = k.shape[0]
+    if k.shape != (nk, d) or v.shape != (nk, d) or dout.shape != (nq, d):
+        raise ValueError("k, v must be [nk, d] and dout [nq, d] with the d of q")
+    if qpos is None:
+        qpos = np.arange(nq, dtype=np.int64)
+    qpos = np.ascontiguousarray(np.asarray(qpos, dtype=np.int64))
+    dq = np.zeros((nq, d), dtype=np.float64)
+    dk = np.zeros((nk, d), dtype=np.float64)
+    dv = np.zeros((nk, d), dtype=np.float64)
+    rc = _load().oracle_attention_bwd_head(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), qpos.ctypes.data_as(_I64), nq, nk, d, float(scale),
+        int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attention_bwd_head rejected its arguments")
+    return dq, dk, dv
+
+
 def kv_head_of(h: int, hq: int, hkv: int) -> int:
     """KV head read by query head ``h`` (contiguous groups of ``hq // hkv``)."""
     if hq % hkv:
@@ -129,6 +157,26 @@ def attention(q, k, v, scale, causal=False, nthreads=0):
             o[b, h], lse[b, h] = attention_head(q[b, h], k[b, g], v[b, g], scale, causal,
                                                 nthreads=nthreads)
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, scale, causal=False, nthreads=0):
+    """Full backward: ``q, dout [B, Hq, N, d]``, ``k, v [B, Hkv, N, d]`` ->
+    ``(dq, dk, dv)``; the gradient of a KV head is the sum over the query
+    heads that read it."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, hq, _, _ = q.shape
+    hkv = k.shape[1]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(hq):
+            g = kv_head_of(h, hq, hkv)
+            dq[b, h], dkh, dvh = attention_bwd_head(q[b, h], k[b, g], v[b, g], dout[b, h], scale,
+                                                    causal, nthreads=nthreads)
+            dk[b, g] += dkh
+            dv[b, g] += dvh
+    return dq, dk, dv
 
 
 def attention_rows(q_rows, k_head, v_head, scale, causal, positions, nthreads=0):

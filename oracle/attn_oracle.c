@@ -32,6 +32,18 @@
  * Everything is computed in double precision.  Rows are spread over POSIX
  * threads; each row's arithmetic is sequential and independent of the
  * thread count.
+ *
+ * The backward pass (oracle_attention_bwd_head) is the gradient of the same
+ * definition by the chain rule, for a loss whose gradient with respect to the
+ * output is dO (the pages measure an FA2 backward pass but print no formula
+ * for it; the gradient of the section-4 equation is fixed by the mathematics):
+ *   dv_j += p_j dO_i                              (O = P V)
+ *   dp_j  = <dO_i, v_j>
+ *   D_i   = <dO_i, o_i> = sum_j p_j dp_j
+ *   ds_j  = p_j (dp_j - D_i)                      (softmax Jacobian)
+ *   dq_i  = scale * sum_j ds_j k_j                (s_j = scale <q_i, k_j>)
+ *   dk_j += scale * ds_j q_i
+ * with p the normalised probabilities of row i over its attended keys.
  */
 #include <math.h>
 #include <pthread.h>
@@ -177,5 +189,131 @@ int oracle_lse_merge(const double *o_parts, const double *lse_parts, int64_t S, 
     }
     for (int64_t c = 0; c < d; ++c) o[c] /= wsum;
     *lse = L + log(wsum);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ backward */
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    const int64_t *qpos;
+    int64_t nq, nk, d;
+    double scale;
+    int causal;
+    double *dq;      /* [nq, d], rows of this job only */
+    double *dk, *dv; /* [nk, d], this job's private sums */
+    double *p;       /* nk doubles of scratch */
+    int64_t row_begin, row_end;
+} grad_job;
+
+/* Gradient contributions of one query row (see the file comment). */
+static void grad_one_row(const grad_job *jb, int64_t i) {
+    const int64_t d = jb->d;
+    const double *qi = jb->q + i * d;
+    const double *gi = jb->dout + i * d;
+    double *dqi = jb->dq + i * d;
+    for (int64_t c = 0; c < d; ++c) dqi[c] = 0.0;
+    int64_t hi = jb->nk;
+    if (jb->causal && jb->qpos[i] + 1 < hi) hi = jb->qpos[i] + 1;
+    if (hi <= 0) return; /* no attended key: the output is the constant 0 */
+    double *p = jb->p;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < hi; ++j) {
+        const double *krow = jb->k + j * d;
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += qi[c] * krow[c];
+        p[j] = jb->scale * dot;
+        if (p[j] > m) m = p[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < hi; ++j) {
+        p[j] = exp(p[j] - m);
+        l += p[j];
+    }
+    for (int64_t j = 0; j < hi; ++j) p[j] /= l;
+    /* D_i = <dO_i, o_i> with o_i = sum_j p_j v_j */
+    double D = 0.0;
+    for (int64_t c = 0; c < d; ++c) {
+        double oc = 0.0;
+        for (int64_t j = 0; j < hi; ++j) oc += p[j] * jb->v[j * d + c];
+        D += gi[c] * oc;
+    }
+    for (int64_t j = 0; j < hi; ++j) {
+        const double *krow = jb->k + j * d;
+        const double *vrow = jb->v + j * d;
+        double dp = 0.0;
+        for (int64_t c = 0; c < d; ++c) dp += gi[c] * vrow[c];
+        const double ds = p[j] * (dp - D);
+        double *dkj = jb->dk + j * d;
+        double *dvj = jb->dv + j * d;
+        for (int64_t c = 0; c < d; ++c) {
+            dqi[c] += jb->scale * ds * krow[c];
+            dkj[c] += jb->scale * ds * qi[c];
+            dvj[c] += p[j] * gi[c];
+        }
+    }
+}
+
+static void *grad_worker(void *arg) {
+    grad_job *jb = (grad_job *)arg;
+    for (int64_t i = jb->row_begin; i < jb->row_end; ++i) grad_one_row(jb, i);
+    return NULL;
+}
+
+/*
+ * Gradients of one head.
+ *   q, dout [nq, d]; k, v [nk, d]; qpos [nq] (used only when causal: key j is
+ *   attended by row i when j <= qpos[i])
+ *   dq [nq, d]; dk, dv [nk, d]   outputs (overwritten)
+ * dk and dv are the sums of the rows' contributions; each thread sums its own
+ * rows and the threads' sums are added in thread order.
+ * Returns 0, or -1 on bad arguments / allocation failure.
+ */
+int oracle_attention_bwd_head(const double *q, const double *k, const double *v,
+                              const double *dout, const int64_t *qpos, int64_t nq, int64_t nk,
+                              int64_t d, double scale, int causal, double *dq, double *dk,
+                              double *dv, int nthreads) {
+    if (nq < 0 || nk < 0 || d <= 0) return -1;
+    if (causal && !qpos) return -1;
+    for (int64_t x = 0; x < nk * d; ++x) dk[x] = dv[x] = 0.0;
+    if (nq == 0) return 0;
+    if (nthreads <= 0) nthreads = oracle_default_threads();
+    if (nthreads > nq) nthreads = (int)nq;
+    const size_t span = (size_t)(nk > 0 ? nk : 1);
+    const size_t kd = (size_t)nk * (size_t)d;
+    double *scratch = (double *)malloc(sizeof(double) * span * (size_t)nthreads);
+    double *acc = (double *)calloc(2 * kd * (size_t)nthreads + 1, sizeof(double));
+    grad_job *jobs = (grad_job *)malloc(sizeof(grad_job) * (size_t)nthreads);
+    pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!scratch || !acc || !jobs || !tids) {
+        free(scratch); free(acc); free(jobs); free(tids);
+        return -1;
+    }
+    int64_t per = (nq + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        grad_job *jb = &jobs[t];
+        jb->q = q; jb->k = k; jb->v = v; jb->dout = dout; jb->qpos = qpos;
+        jb->nq = nq; jb->nk = nk; jb->d = d; jb->scale = scale; jb->causal = causal;
+        jb->dq = dq;
+        jb->dk = acc + 2 * kd * (size_t)t;
+        jb->dv = jb->dk + kd;
+        jb->p = scratch + span * (size_t)t;
+        jb->row_begin = (int64_t)t * per;
+        jb->row_end = jb->row_begin + per < nq ? jb->row_begin + per : nq;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, grad_worker, &jobs[t]) != 0) break;
+        started = t;
+    }
+    grad_worker(&jobs[0]);
+    for (int t = started + 1; t < nthreads; ++t) grad_worker(&jobs[t]);
+    for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+    for (int t = 0; t < nthreads; ++t)
+        for (size_t x = 0; x < kd; ++x) {
+            dk[x] += jobs[t].dk[x];
+            dv[x] += jobs[t].dv[x];
+        }
+    free(scratch); free(acc); free(jobs); free(tids);
     return 0;
 }
