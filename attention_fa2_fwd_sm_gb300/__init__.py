@@ -25,8 +25,10 @@ ATTN_ERR_TIMEOUT = -5
 ORDER_HEAD_FIRST = 0
 ORDER_BLOCK_FIRST = 1
 ORDER_NAIVE_HEAD_FIRST = 2
+ORDER_DIE_SPLIT_HEAD_FIRST = 3
 ORDERS = {"head_first": ORDER_HEAD_FIRST, "block_first": ORDER_BLOCK_FIRST,
-          "naive_head_first": ORDER_NAIVE_HEAD_FIRST}
+          "naive_head_first": ORDER_NAIVE_HEAD_FIRST,
+          "die_split_head_first": ORDER_DIE_SPLIT_HEAD_FIRST}
 
 # Every symbol include/attn.h declares, with (restype, argtypes).
 _P = ctypes.c_void_p
@@ -35,14 +37,19 @@ _F = ctypes.c_float
 _LL = ctypes.c_longlong
 _SZ = ctypes.c_size_t
 _IP = ctypes.POINTER(ctypes.c_int)
+_FP = ctypes.POINTER(ctypes.c_float)
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
+    "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "attn_tile_map": (_I, [_I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
+    "attn_tile_map_die_split": (_I, [_I, _I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
+    "attn_die_map": (_I, [_IP, _I, _FP]),
     "attn_fwd_units": (_LL, [_I, _I, _I]),
     "attn_device_status": (_I, [_P]),
     "attn_set_wait_timeout_ns": (_LL, [_LL]),
@@ -115,6 +122,17 @@ def attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, st
                              float(scale), int(bool(causal)), int(tile_order), _stream(stream))
 
 
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, tile_order,
+             workspace, workspace_bytes, stream=None) -> int:
+    return lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                          _ptr(dv), B, Hq, Hkv, N, d, float(scale), int(bool(causal)), int(tile_order),
+                          _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def attn_bwd_workspace_bytes(B, Hq, N) -> int:
+    return int(lib().attn_bwd_workspace_bytes(B, Hq, N))
+
+
 def attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, num_splits, max_seqlen,
                 workspace=None, workspace_bytes=0, stream=None) -> int:
     return lib().attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), B, Hq,
@@ -148,6 +166,29 @@ def attn_tile_map(tile_order, B, Hq, N, causal, unit):
                              ctypes.byref(b), ctypes.byref(h), ctypes.byref(m))
     check(rc, "attn_tile_map")
     return b.value, h.value, m.value
+
+
+def attn_tile_map_die_split(B, Hq, Hkv, N, causal, die, k):
+    """(b, h, m) of the k-th unit of die `die` under the die-split order, or
+    None when that die has no k-th unit of its own."""
+    b, h, m = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = lib().attn_tile_map_die_split(B, Hq, Hkv, N, int(bool(causal)), int(die), int(k),
+                                       ctypes.byref(b), ctypes.byref(h), ctypes.byref(m))
+    if rc == ATTN_ERR_ARG:
+        return None
+    check(rc, "attn_tile_map_die_split")
+    return b.value, h.value, m.value
+
+
+def attn_die_map(capacity=256):
+    """(die of each SM id, stats) of the current device, as the die-split order
+    uses it; stats = (measured, min |corr|, near clk, far clk)."""
+    dies = (ctypes.c_int * capacity)()
+    stats = (ctypes.c_float * 4)()
+    n = lib().attn_die_map(dies, capacity, stats)
+    if n < 0:
+        check(n, "attn_die_map")
+    return list(dies[:min(n, capacity)]), tuple(stats)
 
 
 def attn_fwd_units(B, Hq, N) -> int:
@@ -184,6 +225,24 @@ def forward(q, k, v, causal=False, scale=None, tile_order=ORDER_HEAD_FIRST, with
     check(attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, stream),
           "attn_fwd_ex")
     return o, lse
+
+
+def backward(q, k, v, o, lse, dout, causal=False, scale=None, tile_order=ORDER_HEAD_FIRST, workspace=None,
+             stream=None):
+    """Allocate gradients (and a workspace when none is given) and run attn_bwd
+    on ``[B, H, N, d]`` bf16 CUDA tensors; returns ``(dq, dk, dv)``."""
+    import torch
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    nbytes = attn_bwd_workspace_bytes(B, Hq, N)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    check(attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, tile_order,
+                   workspace, nbytes, stream), "attn_bwd")
+    return dq, dk, dv
 
 
 def decode(q, kcache, vcache, seqlens, num_splits=0, scale=None, workspace=None, stream=None):

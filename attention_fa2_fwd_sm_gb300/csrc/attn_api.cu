@@ -126,6 +126,25 @@ int attn_tile_map(int tile_order, int B, int Hq, int N, int causal, long long un
     return ATTN_OK;
 }
 
+int attn_tile_map_die_split(int B, int Hq, int Hkv, int N, int causal, int die, long long k, int *b,
+                            int *h, int *m) {
+    if (!b || !h || !m || B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || Hq % Hkv) return ATTN_ERR_ARG;
+    if (die < 0 || die >= kDies) return ATTN_ERR_ARG;
+    const int nb = unit_blocks(N);
+    const long long u = die_split_unit(die, k, B, Hkv, Hq / Hkv, nb);
+    if (u < 0) return ATTN_ERR_ARG;
+    const Tile t = unit_to_tile(kHeadFirst, u, Hq, nb, causal ? 1 : 0);
+    *b = t.b;
+    *h = t.h;
+    *m = t.m;
+    return ATTN_OK;
+}
+
+int attn_die_map(int *die_of_sm, int capacity, float *stats) {
+    if (capacity < 0 || (capacity > 0 && !die_of_sm)) return ATTN_ERR_ARG;
+    return die_map_query(die_of_sm, capacity, stats);
+}
+
 static int validate_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                         int Hq, int Hkv, int N, int d, float scale, int tile_order) {
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_ARG;
@@ -133,7 +152,7 @@ static int validate_fwd(const void *q, const void *k, const void *v, void *o, fl
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0) return ATTN_ERR_ARG;
     if (Hq % Hkv) return ATTN_ERR_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_ARG;
-    if (tile_order < kHeadFirst || tile_order > kNaiveHeadFirst) return ATTN_ERR_ARG;
+    if (tile_order < kHeadFirst || tile_order > kDieSplitHeadFirst) return ATTN_ERR_ARG;
     if (d != 56 && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     // tensor-map limits: each dimension < 2^32, strides < 2^40 bytes
     if ((long long)B * Hq >= (1LL << 31) || (long long)N * d * 2 >= (1LL << 39)) return ATTN_ERR_ARG;
@@ -170,6 +189,47 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, i
              int Hkv, int N, int d, float scale, int causal, attn_stream_t stream) {
     return attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, ATTN_ORDER_HEAD_FIRST,
                        stream);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int Hq, int N) {
+    if (B <= 0 || Hq <= 0 || N <= 0) return 0;
+    return (size_t)B * Hq * (size_t)((N + 127) / 128) * 128 * 2 * sizeof(float);
+}
+
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
+             void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+             int tile_order, void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+    int rc = validate_fwd(q, k, v, dq, nullptr, B, Hq, Hkv, N, d, scale, kHeadFirst);
+    if (rc != ATTN_OK) return rc;
+    if (!aligned16(o) || !aligned16(dout) || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_ARG;
+    if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_ARG;
+    if (tile_order < kHeadFirst || tile_order > kNaiveHeadFirst) return ATTN_ERR_ARG;
+    const size_t need = (size_t)B * Hq * (size_t)((N + 127) / 128) * 128 * 2 * sizeof(float);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    const int sms = current_num_sms();
+    if (sms <= 0) return note_cuda_error(cudaErrorNoDevice, "device query");
+    BwdLaunch a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.order = tile_order;
+    a.workspace = static_cast<float *>(workspace);
+    a.wait_ns = (unsigned long long)g_wait_ns.load();
+    a.num_sms = sms;
+    return bwd_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t attn_decode_workspace_bytes(int B, int Hq, int d, int num_splits) {
@@ -282,10 +342,11 @@ int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, c
 int attn_device_status(attn_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    int a = 0, b = 0;
-    if (fwd_take_status(&a) != cudaSuccess || decode_take_status(&b) != cudaSuccess)
+    int a = 0, b = 0, c = 0;
+    if (fwd_take_status(&a) != cudaSuccess || decode_take_status(&b) != cudaSuccess ||
+        bwd_take_status(&c) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    return (a | b) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    return (a | b | c) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 }  // extern "C"

@@ -20,6 +20,18 @@ struct FwdLaunch {
     int num_sms;
 };
 
+struct BwdLaunch {
+    const void *q, *k, *v, *o, *dout;
+    const float *lse;
+    void *dq, *dk, *dv;
+    int B, Hq, Hkv, N, d;
+    float scale;
+    int causal, order;
+    float *workspace;  // 2 * B * Hq * roundup(N, 128) floats
+    unsigned long long wait_ns;
+    int num_sms;
+};
+
 struct DecodeLaunch {
     const void *q, *kcache, *vcache;
     const int *seqlens;
@@ -37,6 +49,7 @@ int note_cuda_error(cudaError_t e, const char *where);
 // Each returns 0 or a negative ATTN_ERR_* code.
 int fwd_launch(const FwdLaunch &a, cudaStream_t stream);
 int decode_launch(const DecodeLaunch &a, cudaStream_t stream);
+int bwd_launch(const BwdLaunch &a, cudaStream_t stream);
 
 // Size of the built-in scratch array used by attn_decode_noalloc.
 constexpr size_t kDecodeNoAllocScratchBytes = size_t(4) << 20;
@@ -45,10 +58,20 @@ constexpr size_t kDecodeNoAllocScratchBytes = size_t(4) << 20;
 // first call for each device).
 cudaError_t decode_noalloc_scratch(void **ptr);
 
+// SM -> die map of the current device for the die-split order (measured on
+// the first call for each device; see die_map.cu).  die_map_device gives the
+// device address of the map (kDieMapMaxSms ints, one per SM id);
+// die_map_query copies it to the host with the calibration statistics and
+// returns the SM count.  Both return a negative ATTN_ERR_* code on failure.
+constexpr int kDieMapMaxSms = 256;
+int die_map_device(const int **ptr);
+int die_map_query(int *die_of_sm, int capacity, float *stats);
+
 // Read and clear the status word of each kernel translation unit (OR of
 // kStatus* bits).
 cudaError_t fwd_take_status(int *bits);
 cudaError_t decode_take_status(int *bits);
+cudaError_t bwd_take_status(int *bits);
 
 // Tiled bf16 tensor map over a 3-D row-major tensor [dim2][dim1][dim0]
 // (dim0 contiguous), box {box0, box1, 1}, 128-byte swizzle, zero fill out of

@@ -1,0 +1,964 @@
+// bwd_sm103.cu -- FlashAttention-2 style backward pass for sm_103a.
+//
+// Gradients of O = softmax(scale * Q K^T) V ("Optimizing Attention on GPUs by
+// Exploiting GPU Architectural NUMA Effects", detail page, section 4
+// equation; the same pages measure an FA2 backward pass, section 5 "backward
+// pass") for an output gradient dO, by the chain rule:
+//   P = exp(scale * Q K^T - lse)      (lse saved by the forward pass)
+//   dV = P^T dO,   dP = dO V^T,   Delta = rowsum(dO * O)
+//   dS = P * (dP - Delta),   dQ = scale * dS K,   dK = scale * dS^T Q
+// with the causal mask and grouped-query heads as in the forward pass (the
+// gradient of a KV head sums over the query heads that read it).
+//
+// Three kernels, in stream order:
+//   bwd_pre_kernel   Delta and lse * log2(e) per query row, into a padded
+//                    fp32 workspace (+inf / 0 past the last row, which makes
+//                    padded query rows drop out of every product).
+//   dkdv_kernel<D>   one unit = 128 keys of one KV head; K and V stay in shared
+//                    memory while the query blocks of every query head of the
+//                    group stream through a TMA ring (with their lse and Delta):
+//                    S^T = K Q^T and dP^T = V dO^T (SS MMAs into TMEM), P^T
+//                    and dS^T in bf16 written back over them, then dV += P^T dO
+//                    and dK += dS^T Q (TS MMAs, dO and Q read MN-major).
+//   dq_kernel<D>     one unit = 128 query rows of one query head; Q and dO stay
+//                    in shared memory while K/V blocks stream: S = Q K^T and
+//                    dP = dO V^T, dS in bf16 over S, dQ += dS K (TS MMA).
+// Splitting dQ into its own pass recomputes S and dP (seven products instead of
+// five) but needs no atomic accumulation: every output element is written
+// once, by one CTA, and the result does not depend on the schedule.
+//
+// Both main kernels are persistent (one CTA per SM) and take units from an
+// atomic counter in the chosen order.  Head-first keeps the CTAs that run at
+// the same time on one Attention Compute Cluster, so the operand they all
+// stream (the group's Q/dO in dkdv, the head's K/V in dq) is read from HBM
+// about once and then served by L2 (detail page, section 2 Q2).
+// Roles (256 threads): warp 0 TMA producer, warp 1 tcgen05 issuer and TMEM
+// owner, warps 2-3 idle, warps 4-7 elementwise / epilogue (warp w owns TMEM
+// lanes [32 (w % 4), +32): one row of the tile per thread).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+#include "tile_order.cuh"
+
+namespace attn {
+
+static __device__ int g_bwd_status;
+
+// Work counters (as in the forward kernel): per launch slot and kernel
+// {next unit, CTAs finished}; the last CTA of a launch resets its pair.
+constexpr int kBwdSchedSlots = 64;
+static __device__ unsigned int g_bwd_work[kBwdSchedSlots][2][2];
+
+namespace bwd {
+
+constexpr int kRows = 128;     // rows per tile (keys in dkdv, queries in dq)
+constexpr int kThreads = 256;  // 8 warps
+constexpr int kTmemCols = 512;
+
+struct Params {
+    __nv_bfloat16 *out0, *out1;  // dkdv: dK, dV; dq: dQ (out1 unused)
+    const float *lse2;           // [B*Hq, npad]  lse * log2(e), +inf past N
+    const float *delta;          // [B*Hq, npad]  rowsum(dO * O), 0 past N
+    int B, N, npad, Hq, Hkv, G, d_store, causal, order, nblk;
+    long long total_units;
+    float scale, scale_log2;
+    unsigned long long wait_ns;
+    int sched_slot;
+};
+
+// ------------------------------------------------------------------ pre-pass
+
+// One warp per padded query row: Delta = sum_c dO[c] * O[c] (fp32) and
+// lse * log2(e); rows at or past N get +inf and 0.
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
+                                                      const __nv_bfloat16 *__restrict__ dout,
+                                                      const float *__restrict__ lse, float *lse2,
+                                                      float *delta, int N, int npad, int d,
+                                                      long long rows) {
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+         r += warps) {
+        const long long bh = r / npad;
+        const int n = int(r % npad);
+        if (n >= N) {
+            if (lane == 0) {
+                lse2[r] = INFINITY;
+                delta[r] = 0.f;
+            }
+            continue;
+        }
+        const size_t base = ((size_t)bh * N + n) * d;
+        float acc = 0.f;
+        for (int c = 2 * lane; c < d; c += 64) {
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o + base + c);
+            const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162 *>(dout + base + c);
+            const float2 af = __bfloat1622float2(a), gf = __bfloat1622float2(g);
+            acc = fmaf(af.x, gf.x, acc);
+            acc = fmaf(af.y, gf.y, acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            lse2[r] = lse[(size_t)bh * N + n] * 1.4426950408889634f;
+            delta[r] = acc;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ schedule
+
+// dkdv unit -> (b, kv head g, key block j).  Head-first: j fastest (causal:
+// ascending, so the blocks with the most query rows start first).
+// Block-first: (b, g) fastest.
+struct KvUnit {
+    int b, g, j;
+};
+__device__ __forceinline__ KvUnit kv_unit(const Params &p, long long u) {
+    KvUnit w;
+    const int nbg = p.B * p.Hkv;
+    if (p.order == kBlockFirst) {
+        const int bg = int(u % nbg);
+        w.j = int(u / nbg);
+        w.b = bg / p.Hkv;
+        w.g = bg % p.Hkv;
+    } else {
+        w.j = int(u % p.nblk);
+        const long long bg = u / p.nblk;
+        w.g = int(bg % p.Hkv);
+        w.b = int(bg / p.Hkv);
+    }
+    return w;
+}
+
+// dq unit -> (b, query head h, query block i): the forward pass's unit map
+// with 128-row blocks (causal: descending i, longest first).
+struct QUnit {
+    int b, h, i;
+};
+__device__ __forceinline__ QUnit q_unit(const Params &p, long long u) {
+    QUnit w;
+    int r;
+    if (p.order == kBlockFirst) {
+        w.h = int(u % p.Hq);
+        const long long bm = u / p.Hq;
+        r = int(bm % p.nblk);
+        w.b = int(bm / p.nblk);
+    } else {
+        r = int(u % p.nblk);
+        const long long bh = u / p.nblk;
+        w.h = int(bh % p.Hq);
+        w.b = int(bh / p.Hq);
+    }
+    w.i = p.causal ? (p.nblk - 1 - r) : r;
+    return w;
+}
+
+// The i-th unit of this CTA (naive head-first: the CTA's own index), or -1.
+__device__ __forceinline__ long long fetch_unit(const Params &p, int kernel, long long i) {
+    if (p.order == kNaiveHeadFirst) return i == 0 ? (long long)blockIdx.x : -1;
+    const unsigned int u = atomicAdd(&g_bwd_work[p.sched_slot][kernel][0], 1u);
+    return (long long)u < p.total_units ? (long long)u : -1;
+}
+
+__device__ __forceinline__ void finish_schedule(const Params &p, int kernel) {
+    if (threadIdx.x == 0 && p.order != kNaiveHeadFirst) {
+        __threadfence();
+        const unsigned int done = atomicAdd(&g_bwd_work[p.sched_slot][kernel][1], 1u);
+        if (done == gridDim.x - 1) {
+            atomicExch(&g_bwd_work[p.sched_slot][kernel][0], 0u);
+            atomicExch(&g_bwd_work[p.sched_slot][kernel][1], 0u);
+        }
+    }
+}
+
+// Store one row of a TMEM accumulator (D fp32 columns at `t_row`) to global
+// memory as bf16, multiplied by `mul`; columns at or past d_store are clipped.
+template <int D>
+__device__ __forceinline__ void store_row(uint32_t t_row, __nv_bfloat16 *dst, bool row_ok, int d_store,
+                                          float mul) {
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(t_row + c * 32, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+        if (row_ok) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int col = c * 32 + g * 8;
+                if (col < d_store)
+                    *reinterpret_cast<uint4 *>(dst + col) =
+                        make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            }
+        }
+    }
+}
+
+// A 1-D bulk copy global -> shared memory completing on an mbarrier (both
+// addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+
+// ------------------------------------------------------------------- dK, dV
+
+template <int D>
+struct KvCfg {
+    static constexpr int kChunks = D / 64;             // 128-byte column chunks of a row
+    static constexpr int kChunkBytes = kRows * 128;    // one chunk of 128 rows
+    static constexpr int kTileBytes = kRows * D * 2;   // one 128 x D bf16 tile
+    static constexpr int kStages = (D == 128) ? 2 : 3; // Q/dO ring
+    static constexpr int kStageBytes = 2 * kTileBytes + 1024;  // Q, dO, lse2, Delta
+    // barriers: kv_full kv_empty st_full[S] st_empty[S] s_full p_full acc_full
+    //           acc_empty uq_full[2] uq_empty[2] drain
+    static constexpr int kBarKVFull = 0, kBarKVEmpty = 1, kBarStFull = 2, kBarStEmpty = 2 + kStages,
+                         kBarSFull = 2 + 2 * kStages, kBarPFull = 3 + 2 * kStages,
+                         kBarAccFull = 4 + 2 * kStages, kBarAccEmpty = 5 + 2 * kStages,
+                         kBarUQFull = 6 + 2 * kStages, kBarUQEmpty = 8 + 2 * kStages,
+                         kBarDrain = 10 + 2 * kStages, kNumBars = 11 + 2 * kStages;
+    static constexpr int kDataBytes = 2 * kTileBytes + kStages * kStageBytes;
+    static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 32 + 1024;
+    static constexpr int kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+};
+
+// Query blocks per query head that key block j meets (causal: i >= j).
+__device__ __forceinline__ int kv_first_i(const Params &p, int j) { return p.causal ? j : 0; }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const Params p) {
+    using C = KvCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *sK = smem;
+    uint8_t *sV = smem + C::kTileBytes;
+    uint8_t *sStage = smem + 2 * C::kTileBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kDataBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *unit_q = reinterpret_cast<volatile int *>(tmem_slot + 2);  // 2 entries
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+    auto stage_q = [&](int s) { return sStage + s * C::kStageBytes; };
+    auto stage_do = [&](int s) { return sStage + s * C::kStageBytes + C::kTileBytes; };
+    auto stage_l = [&](int s) {
+        return reinterpret_cast<const float *>(sStage + s * C::kStageBytes + 2 * C::kTileBytes);
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::kBarKVFull), 1);
+        mbar_init(bar(C::kBarKVEmpty), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar(C::kBarStFull + s), 1);
+            mbar_init(bar(C::kBarStEmpty + s), 1 + 4);  // MMA commit + 4 elementwise warps
+        }
+        mbar_init(bar(C::kBarSFull), 1);
+        mbar_init(bar(C::kBarPFull), 4);
+        mbar_init(bar(C::kBarAccFull), 1);
+        mbar_init(bar(C::kBarAccEmpty), 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::kBarUQFull + i), 1);
+            mbar_init(bar(C::kBarUQEmpty + i), 1 + 4);  // MMA thread + 4 elementwise warps
+        }
+        mbar_init(bar(C::kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmDO);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    int *status = &g_bwd_status;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            long long fills = 0;  // ring fills issued
+            int kv_loads = 0;
+            bool ok = true;
+            for (long long qi = 0; ok; ++qi) {
+                const long long u = fetch_unit(p, 0, qi);
+                const int qs = int(qi & 1);
+                if (qi >= 2 && !mbar_wait_bounded(bar(C::kBarUQEmpty + qs), uint32_t(((qi >> 1) - 1) & 1),
+                                                  p.wait_ns, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                unit_q[qs] = int(u);
+                mbar_arrive(bar(C::kBarUQFull + qs));
+                if (u < 0) break;
+                const KvUnit w = kv_unit(p, u);
+                if (kv_loads > 0 && !mbar_wait_bounded(bar(C::kBarKVEmpty), uint32_t((kv_loads - 1) & 1),
+                                                       p.wait_ns, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(C::kBarKVFull), 2 * C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(smem_u32(sK + c * C::kChunkBytes), &tmK, bar(C::kBarKVFull), c * 64,
+                                w.j * kRows, w.b * p.Hkv + w.g);
+                    tma_load_3d(smem_u32(sV + c * C::kChunkBytes), &tmV, bar(C::kBarKVFull), c * 64,
+                                w.j * kRows, w.b * p.Hkv + w.g);
+                }
+                ++kv_loads;
+                const int i0 = kv_first_i(p, w.j);
+                const int ni = p.nblk - i0;
+                const int iters = p.G * ni;
+                for (int t = 0; t < iters; ++t) {
+                    const int h = w.g * p.G + t / ni;
+                    const int i = i0 + t % ni;
+                    const int slot = int(fills % C::kStages);
+                    const long long round = fills / C::kStages;
+                    if (round > 0 && !mbar_wait_bounded(bar(C::kBarStEmpty + slot), uint32_t((round - 1) & 1),
+                                                        p.wait_ns, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar(C::kBarStFull + slot);
+                    mbar_arrive_expect_tx(fb, 2 * C::kTileBytes + 1024);
+                    const int bh = w.b * p.Hq + h;
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_3d(smem_u32(stage_q(slot) + c * C::kChunkBytes), &tmQ, fb, c * 64, i * kRows,
+                                    bh);
+                        tma_load_3d(smem_u32(stage_do(slot) + c * C::kChunkBytes), &tmDO, fb, c * 64,
+                                    i * kRows, bh);
+                    }
+                    const size_t row0 = (size_t)bh * p.npad + (size_t)i * kRows;
+                    bulk_load(smem_u32(stage_l(slot)), p.lse2 + row0, kRows * 4, fb);
+                    bulk_load(smem_u32(stage_l(slot) + kRows), p.delta + row0, kRows * 4, fb);
+                    ++fills;
+                }
+            }
+            if (!ok) {
+                // Drain: wait (bounded, independent of the caller's limit) for the
+                // last fill of every slot and the last K/V load, so no copy is
+                // still writing shared memory when the CTA exits.
+                const unsigned long long drain_ns = 1000000000ull;
+                volatile int no_abort = 0;
+                for (int s = 0; s < C::kStages; ++s) {
+                    if (fills <= s) continue;
+                    const long long last = fills - 1 - ((fills - 1 - s) % C::kStages);
+                    if (!mbar_wait_bounded(bar(C::kBarStFull + s), uint32_t((last / C::kStages) & 1), drain_ns,
+                                           &no_abort, status))
+                        atomicOr(status, kStatusDrainTimeout);
+                }
+                if (kv_loads > 0 && !mbar_wait_bounded(bar(C::kBarKVFull), uint32_t((kv_loads - 1) & 1),
+                                                       drain_ns, &no_abort, status))
+                    atomicOr(status, kStatusDrainTimeout);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16_f32(kRows, kRows, 0);  // K-major A and B
+            constexpr uint32_t kIdescAcc = idesc_bf16_f32(kRows, D, 1);    // B read MN-major
+            const uint64_t dK0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t dV0 = smem_desc_sw128(smem_u32(sV), 16, 1024);
+            long long fills = 0;
+            int kv_used = 0, p_waits = 0, units_done = 0;
+            bool ok = true;
+            for (long long qi = 0; ok; ++qi) {
+                const int qs = int(qi & 1);
+                ok = mbar_wait_bounded(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag,
+                                       status);
+                if (!ok) break;
+                const long long u = unit_q[qs];
+                mbar_arrive(bar(C::kBarUQEmpty + qs));
+                if (u < 0) break;
+                const KvUnit w = kv_unit(p, u);
+                const int iters = p.G * (p.nblk - kv_first_i(p, w.j));
+                ok = mbar_wait_bounded(bar(C::kBarKVFull), uint32_t(kv_used & 1), p.wait_ns, abort_flag, status);
+                if (!ok) break;
+                ++kv_used;
+                for (int t = 0; ok && t < iters; ++t) {
+                    const int slot = int(fills % C::kStages);
+                    ok = mbar_wait_bounded(bar(C::kBarStFull + slot), uint32_t((fills / C::kStages) & 1),
+                                           p.wait_ns, abort_flag, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t dQk = smem_desc_sw128(smem_u32(stage_q(slot)), 16, 1024);
+                    const uint64_t dOk = smem_desc_sw128(smem_u32(stage_do(slot)), 16, 1024);
+                    // S^T = K Q^T and dP^T = V dO^T (K steps over the head dimension)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
+                        tc_mma_ss(tmem_base + C::kColS, dK0 + off, dQk + off, kIdescS, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
+                        tc_mma_ss(tmem_base + C::kColDP, dV0 + off, dOk + off, kIdescS, kk > 0);
+                    }
+                    tc_commit(bar(C::kBarSFull));
+                    ok = mbar_wait_bounded(bar(C::kBarPFull), uint32_t(p_waits & 1), p.wait_ns, abort_flag, status);
+                    if (!ok) break;
+                    ++p_waits;
+                    if (t == 0 && units_done > 0) {
+                        ok = mbar_wait_bounded(bar(C::kBarAccEmpty), uint32_t((units_done - 1) & 1), p.wait_ns,
+                                               abort_flag, status);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    // dV += P^T dO and dK += dS^T Q (K steps over the 128 query rows;
+                    // P^T / dS^T bf16 in TMEM, dO / Q read MN-major)
+                    const uint64_t dOmn = smem_desc_sw128(smem_u32(stage_do(slot)), C::kChunkBytes, 1024);
+                    const uint64_t dQmn = smem_desc_sw128(smem_u32(stage_q(slot)), C::kChunkBytes, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        tc_mma_ts(tmem_base + C::kColDV, tmem_base + C::kColS + kk * 8,
+                                  dOmn + uint64_t((kk * 16 * 128) >> 4), kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        tc_mma_ts(tmem_base + C::kColDK, tmem_base + C::kColDP + kk * 8,
+                                  dQmn + uint64_t((kk * 16 * 128) >> 4), kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar(C::kBarStEmpty + slot));
+                    ++fills;
+                    if (t == iters - 1) {
+                        tc_commit(bar(C::kBarAccFull));
+                        tc_commit(bar(C::kBarKVEmpty));
+                        ++units_done;
+                    }
+                }
+            }
+            tc_commit(bar(C::kBarDrain));
+            volatile int no_abort = 0;
+            if (!mbar_wait_bounded(bar(C::kBarDrain), 0, 1000000000ull, &no_abort, status))
+                atomicOr(status, kStatusDrainTimeout);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- elementwise / epilogue
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // key row inside the block
+        const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        const uint32_t tS = tmem_base + lane_off + C::kColS;
+        const uint32_t tDP = tmem_base + lane_off + C::kColDP;
+        const float sl2 = p.scale_log2;
+        long long fills = 0;
+        int s_waits = 0, acc_waits = 0;
+        bool ok = true;
+        for (long long qi = 0; ok; ++qi) {
+            const int qs = int(qi & 1);
+            ok = mbar_wait_warp(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag, status);
+            if (!ok) break;
+            const long long u = unit_q[qs];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarUQEmpty + qs));
+            if (u < 0) break;
+            const KvUnit w = kv_unit(p, u);
+            const int i0 = kv_first_i(p, w.j);
+            const int ni = p.nblk - i0;
+            const int iters = p.G * ni;
+            for (int t = 0; t < iters; ++t) {
+                const int i = i0 + t % ni;
+                const int slot = int(fills % C::kStages);
+                ok = mbar_wait_warp(bar(C::kBarSFull), uint32_t(s_waits & 1), p.wait_ns, abort_flag, status);
+                // The stage's lse / Delta rows: wait on the stage's own fill barrier
+                // (already complete, since the MMA thread waited on it first).
+                if (ok)
+                    ok = mbar_wait_warp(bar(C::kBarStFull + slot), uint32_t((fills / C::kStages) & 1), p.wait_ns,
+                                        abort_flag, status);
+                if (!ok) break;
+                ++s_waits;
+                tc_fence_after();
+                const float4 *l4 = reinterpret_cast<const float4 *>(stage_l(slot));
+                const float4 *d4 = reinterpret_cast<const float4 *>(stage_l(slot) + kRows);
+                const bool diag = p.causal && i == w.j;  // query rows before this key are masked
+#pragma unroll
+                for (int c = 0; c < kRows / 32; ++c) {
+                    uint32_t sv[32], dv[32];
+                    tmem_ld32(tS + c * 32, sv);
+                    tmem_ld32(tDP + c * 32, dv);
+                    tmem_wait_ld();
+                    uint32_t pk[16], dk[16];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 L = l4[c * 8 + e];
+                        const float4 Dl = d4[c * 8 + e];
+                        const float lv[4] = {L.x, L.y, L.z, L.w};
+                        const float dl[4] = {Dl.x, Dl.y, Dl.z, Dl.w};
+                        float pr[4], ds[4];
+#pragma unroll
+                        for (int k = 0; k < 4; k += 2) {
+                            float x0, x1;
+                            ffma2(x0, x1, __uint_as_float(sv[4 * e + k]), __uint_as_float(sv[4 * e + k + 1]), sl2,
+                                  sl2, -lv[k], -lv[k + 1]);
+                            pr[k] = fast_exp2(x0);
+                            pr[k + 1] = fast_exp2(x1);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (diag && c * 32 + 4 * e + k < r) pr[k] = 0.f;
+                            ds[k] = pr[k] * (__uint_as_float(dv[4 * e + k]) - dl[k]);
+                        }
+                        pk[2 * e] = pack_bf16x2(pr[0], pr[1]);
+                        pk[2 * e + 1] = pack_bf16x2(pr[2], pr[3]);
+                        dk[2 * e] = pack_bf16x2(ds[0], ds[1]);
+                        dk[2 * e + 1] = pack_bf16x2(ds[2], ds[3]);
+                    }
+                    tmem_st16(tS + c * 16, pk);
+                    tmem_st16(tDP + c * 16, dk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(C::kBarPFull));
+                    mbar_arrive(bar(C::kBarStEmpty + slot));
+                }
+                ++fills;
+            }
+            if (!ok) break;
+            // Epilogue: dV and scale * dK of this thread's key row -> bf16.
+            ok = mbar_wait_warp(bar(C::kBarAccFull), uint32_t(acc_waits & 1), p.wait_ns, abort_flag, status);
+            if (!ok) break;
+            ++acc_waits;
+            tc_fence_after();
+            const int key = w.j * kRows + r;
+            const bool row_ok = key < p.N;
+            const size_t off = ((size_t)(w.b * p.Hkv + w.g) * p.N + (row_ok ? key : 0)) * p.d_store;
+            store_row<D>(tmem_base + lane_off + C::kColDV, p.out1 + off, row_ok, p.d_store, 1.f);
+            store_row<D>(tmem_base + lane_off + C::kColDK, p.out0 + off, row_ok, p.d_store, p.scale);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarAccEmpty));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+    finish_schedule(p, 0);
+}
+
+// ---------------------------------------------------------------------- dQ
+
+template <int D>
+struct QCfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kChunkBytes = kRows * 128;
+    static constexpr int kTileBytes = kRows * D * 2;
+    static constexpr int kStages = (D == 128) ? 2 : 4;  // K/V ring (one stage = K_j and V_j)
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    // barriers: q_full q_empty kv_full[S] kv_empty[S] s_full p_full acc_full
+    //           acc_empty uq_full[2] uq_empty[2] drain
+    static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKVFull = 2, kBarKVEmpty = 2 + kStages,
+                         kBarSFull = 2 + 2 * kStages, kBarPFull = 3 + 2 * kStages,
+                         kBarAccFull = 4 + 2 * kStages, kBarAccEmpty = 5 + 2 * kStages,
+                         kBarUQFull = 6 + 2 * kStages, kBarUQEmpty = 8 + 2 * kStages,
+                         kBarDrain = 10 + 2 * kStages, kNumBars = 11 + 2 * kStages;
+    static constexpr int kDataBytes = 2 * kTileBytes + kStages * kStageBytes;
+    static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 32 + 1024;
+    static constexpr int kColS = 0, kColDP = 128, kColDQ = 256;
+};
+
+// Key blocks query block i meets (causal: j <= i).
+__device__ __forceinline__ int q_nkv(const Params &p, int i) { return p.causal ? i + 1 : p.nblk; }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+              const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+              const Params p) {
+    using C = QCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sDO = smem + C::kTileBytes;
+    uint8_t *sStage = smem + 2 * C::kTileBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kDataBytes);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *unit_q = reinterpret_cast<volatile int *>(tmem_slot + 2);  // 2 entries
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+    auto stage_k = [&](int s) { return sStage + s * C::kStageBytes; };
+    auto stage_v = [&](int s) { return sStage + s * C::kStageBytes + C::kTileBytes; };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::kBarQFull), 1);
+        mbar_init(bar(C::kBarQEmpty), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar(C::kBarKVFull + s), 1);
+            mbar_init(bar(C::kBarKVEmpty + s), 1);
+        }
+        mbar_init(bar(C::kBarSFull), 1);
+        mbar_init(bar(C::kBarPFull), 4);
+        mbar_init(bar(C::kBarAccFull), 1);
+        mbar_init(bar(C::kBarAccEmpty), 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::kBarUQFull + i), 1);
+            mbar_init(bar(C::kBarUQEmpty + i), 1 + 4);
+        }
+        mbar_init(bar(C::kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmDO);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    int *status = &g_bwd_status;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            long long fills = 0;
+            int q_loads = 0;
+            bool ok = true;
+            for (long long qi = 0; ok; ++qi) {
+                const long long u = fetch_unit(p, 1, qi);
+                const int qs = int(qi & 1);
+                if (qi >= 2 && !mbar_wait_bounded(bar(C::kBarUQEmpty + qs), uint32_t(((qi >> 1) - 1) & 1),
+                                                  p.wait_ns, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                unit_q[qs] = int(u);
+                mbar_arrive(bar(C::kBarUQFull + qs));
+                if (u < 0) break;
+                const QUnit w = q_unit(p, u);
+                const int bh = w.b * p.Hq + w.h;
+                if (q_loads > 0 && !mbar_wait_bounded(bar(C::kBarQEmpty), uint32_t((q_loads - 1) & 1), p.wait_ns,
+                                                      abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(C::kBarQFull), 2 * C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(smem_u32(sQ + c * C::kChunkBytes), &tmQ, bar(C::kBarQFull), c * 64, w.i * kRows, bh);
+                    tma_load_3d(smem_u32(sDO + c * C::kChunkBytes), &tmDO, bar(C::kBarQFull), c * 64, w.i * kRows,
+                                bh);
+                }
+                ++q_loads;
+                const int kvh = w.b * p.Hkv + w.h / p.G;
+                const int nkv = q_nkv(p, w.i);
+                for (int j = 0; j < nkv; ++j) {
+                    const int slot = int(fills % C::kStages);
+                    const long long round = fills / C::kStages;
+                    if (round > 0 && !mbar_wait_bounded(bar(C::kBarKVEmpty + slot), uint32_t((round - 1) & 1),
+                                                        p.wait_ns, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar(C::kBarKVFull + slot);
+                    mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_3d(smem_u32(stage_k(slot) + c * C::kChunkBytes), &tmK, fb, c * 64, j * kRows, kvh);
+                        tma_load_3d(smem_u32(stage_v(slot) + c * C::kChunkBytes), &tmV, fb, c * 64, j * kRows, kvh);
+                    }
+                    ++fills;
+                }
+            }
+            if (!ok) {
+                const unsigned long long drain_ns = 1000000000ull;
+                volatile int no_abort = 0;
+                for (int s = 0; s < C::kStages; ++s) {
+                    if (fills <= s) continue;
+                    const long long last = fills - 1 - ((fills - 1 - s) % C::kStages);
+                    if (!mbar_wait_bounded(bar(C::kBarKVFull + s), uint32_t((last / C::kStages) & 1), drain_ns,
+                                           &no_abort, status))
+                        atomicOr(status, kStatusDrainTimeout);
+                }
+                if (q_loads > 0 && !mbar_wait_bounded(bar(C::kBarQFull), uint32_t((q_loads - 1) & 1), drain_ns,
+                                                      &no_abort, status))
+                    atomicOr(status, kStatusDrainTimeout);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16_f32(kRows, kRows, 0);
+            constexpr uint32_t kIdescAcc = idesc_bf16_f32(kRows, D, 1);
+            const uint64_t dQ0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dO0 = smem_desc_sw128(smem_u32(sDO), 16, 1024);
+            long long fills = 0;
+            int q_used = 0, p_waits = 0, units_done = 0;
+            bool ok = true;
+            for (long long qi = 0; ok; ++qi) {
+                const int qs = int(qi & 1);
+                ok = mbar_wait_bounded(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag,
+                                       status);
+                if (!ok) break;
+                const long long u = unit_q[qs];
+                mbar_arrive(bar(C::kBarUQEmpty + qs));
+                if (u < 0) break;
+                const QUnit w = q_unit(p, u);
+                const int nkv = q_nkv(p, w.i);
+                ok = mbar_wait_bounded(bar(C::kBarQFull), uint32_t(q_used & 1), p.wait_ns, abort_flag, status);
+                if (!ok) break;
+                ++q_used;
+                for (int j = 0; ok && j < nkv; ++j) {
+                    const int slot = int(fills % C::kStages);
+                    ok = mbar_wait_bounded(bar(C::kBarKVFull + slot), uint32_t((fills / C::kStages) & 1), p.wait_ns,
+                                           abort_flag, status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t dKk = smem_desc_sw128(smem_u32(stage_k(slot)), 16, 1024);
+                    const uint64_t dVk = smem_desc_sw128(smem_u32(stage_v(slot)), 16, 1024);
+                    // S = Q K^T and dP = dO V^T
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
+                        tc_mma_ss(tmem_base + C::kColS, dQ0 + off, dKk + off, kIdescS, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
+                        tc_mma_ss(tmem_base + C::kColDP, dO0 + off, dVk + off, kIdescS, kk > 0);
+                    }
+                    tc_commit(bar(C::kBarSFull));
+                    ok = mbar_wait_bounded(bar(C::kBarPFull), uint32_t(p_waits & 1), p.wait_ns, abort_flag, status);
+                    if (!ok) break;
+                    ++p_waits;
+                    if (j == 0 && units_done > 0) {
+                        ok = mbar_wait_bounded(bar(C::kBarAccEmpty), uint32_t((units_done - 1) & 1), p.wait_ns,
+                                               abort_flag, status);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    // dQ += dS K (dS bf16 in TMEM over S; K read MN-major)
+                    const uint64_t dKmn = smem_desc_sw128(smem_u32(stage_k(slot)), C::kChunkBytes, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kRows / 16; ++kk)
+                        tc_mma_ts(tmem_base + C::kColDQ, tmem_base + C::kColS + kk * 8,
+                                  dKmn + uint64_t((kk * 16 * 128) >> 4), kIdescAcc, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar(C::kBarKVEmpty + slot));
+                    ++fills;
+                    if (j == nkv - 1) {
+                        tc_commit(bar(C::kBarAccFull));
+                        tc_commit(bar(C::kBarQEmpty));
+                        ++units_done;
+                    }
+                }
+            }
+            tc_commit(bar(C::kBarDrain));
+            volatile int no_abort = 0;
+            if (!mbar_wait_bounded(bar(C::kBarDrain), 0, 1000000000ull, &no_abort, status))
+                atomicOr(status, kStatusDrainTimeout);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- elementwise / epilogue
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // query row inside the block
+        const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+        const uint32_t tS = tmem_base + lane_off + C::kColS;
+        const uint32_t tDP = tmem_base + lane_off + C::kColDP;
+        const float sl2 = p.scale_log2;
+        int s_waits = 0, acc_waits = 0;
+        bool ok = true;
+        for (long long qi = 0; ok; ++qi) {
+            const int qs = int(qi & 1);
+            ok = mbar_wait_warp(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag, status);
+            if (!ok) break;
+            const long long u = unit_q[qs];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarUQEmpty + qs));
+            if (u < 0) break;
+            const QUnit w = q_unit(p, u);
+            const int nkv = q_nkv(p, w.i);
+            const int row = w.i * kRows + r;
+            const size_t prow = (size_t)(w.b * p.Hq + w.h) * p.npad + row;  // row < npad always
+            const float neg_l = -p.lse2[prow];                               // -inf past N
+            const float del = p.delta[prow];
+            for (int j = 0; j < nkv; ++j) {
+                ok = mbar_wait_warp(bar(C::kBarSFull), uint32_t(s_waits & 1), p.wait_ns, abort_flag, status);
+                if (!ok) break;
+                ++s_waits;
+                tc_fence_after();
+                const int kv0 = j * kRows;
+                const bool ragged = kv0 + kRows > p.N;
+                const bool diag = p.causal && j == w.i;
+                int lim = kRows;  // keys kv0 + c with c >= lim are masked
+                if (ragged) lim = p.N - kv0;
+                if (diag) lim = min(lim, r + 1);
+#pragma unroll
+                for (int c = 0; c < kRows / 32; ++c) {
+                    uint32_t sv[32], dv[32];
+                    tmem_ld32(tS + c * 32, sv);
+                    tmem_ld32(tDP + c * 32, dv);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float x0, x1;
+                        ffma2(x0, x1, __uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]), sl2, sl2, neg_l,
+                              neg_l);
+                        float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                        if (c * 32 + 2 * e >= lim) p0 = 0.f;
+                        if (c * 32 + 2 * e + 1 >= lim) p1 = 0.f;
+                        pk[e] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * e]) - del),
+                                            p1 * (__uint_as_float(dv[2 * e + 1]) - del));
+                    }
+                    tmem_st16(tS + c * 16, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarPFull));
+            }
+            if (!ok) break;
+            ok = mbar_wait_warp(bar(C::kBarAccFull), uint32_t(acc_waits & 1), p.wait_ns, abort_flag, status);
+            if (!ok) break;
+            ++acc_waits;
+            tc_fence_after();
+            const bool row_ok = row < p.N;
+            const size_t off = ((size_t)(w.b * p.Hq + w.h) * p.N + (row_ok ? row : 0)) * p.d_store;
+            store_row<D>(tmem_base + lane_off + C::kColDQ, p.out0 + off, row_ok, p.d_store, p.scale);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarAccEmpty));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+    finish_schedule(p, 1);
+}
+
+template <int D>
+int launch(const BwdLaunch &a, cudaStream_t stream) {
+    using CA = KvCfg<D>;
+    using CB = QCfg<D>;
+    const int nblk = (a.N + kRows - 1) / kRows;
+    const int npad = nblk * kRows;
+    const long long rows = (long long)a.B * a.Hq * npad;
+    float *lse2 = a.workspace;
+    float *delta = a.workspace + rows;
+
+    // Pre-pass: Delta and lse * log2(e).
+    {
+        long long blocks = (rows + 7) / 8;
+        const long long cap = (long long)a.num_sms * 16;
+        if (blocks > cap) blocks = cap;
+        bwd_pre_kernel<<<unsigned(blocks), 256, 0, stream>>>(
+            reinterpret_cast<const __nv_bfloat16 *>(a.o), reinterpret_cast<const __nv_bfloat16 *>(a.dout), a.lse,
+            lse2, delta, a.N, npad, a.d, rows);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return note_cuda_error(e, "bwd_pre_kernel launch");
+    }
+
+    CUtensorMap mq, mdo, mk, mv;
+    const uint64_t dd = uint64_t(a.d);
+    if (!encode_bf16_3d(&mq, a.q, dd, uint64_t(a.N), uint64_t(a.B) * a.Hq, 64, kRows) ||
+        !encode_bf16_3d(&mdo, a.dout, dd, uint64_t(a.N), uint64_t(a.B) * a.Hq, 64, kRows) ||
+        !encode_bf16_3d(&mk, a.k, dd, uint64_t(a.N), uint64_t(a.B) * a.Hkv, 64, kRows) ||
+        !encode_bf16_3d(&mv, a.v, dd, uint64_t(a.N), uint64_t(a.B) * a.Hkv, 64, kRows))
+        return note_cuda_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled (backward)");
+
+    static bool attr_set = false;  // per instantiation
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             CA::kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CB::kSmemBytes);
+        if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(backward kernels)");
+        attr_set = true;
+    }
+    static std::atomic<unsigned int> launch_seq{0};
+
+    Params p;
+    p.lse2 = lse2;
+    p.delta = delta;
+    p.B = a.B;
+    p.N = a.N;
+    p.npad = npad;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.d_store = a.d;
+    p.causal = a.causal ? 1 : 0;
+    p.order = a.order;
+    p.nblk = nblk;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.wait_ns = a.wait_ns;
+    p.sched_slot = int(launch_seq.fetch_add(1) % kBwdSchedSlots);
+
+    // dK, dV
+    p.out0 = reinterpret_cast<__nv_bfloat16 *>(a.dk);
+    p.out1 = reinterpret_cast<__nv_bfloat16 *>(a.dv);
+    p.total_units = (long long)a.B * a.Hkv * nblk;
+    long long grid = p.total_units;
+    if (a.order != kNaiveHeadFirst && grid > a.num_sms) grid = a.num_sms;
+    if (grid > 0x7fffffffLL) return -2;
+    dkdv_kernel<D><<<unsigned(grid), kThreads, CA::kSmemBytes, stream>>>(mq, mdo, mk, mv, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return note_cuda_error(e, "dkdv_kernel launch");
+
+    // dQ
+    p.out0 = reinterpret_cast<__nv_bfloat16 *>(a.dq);
+    p.out1 = nullptr;
+    p.total_units = (long long)a.B * a.Hq * nblk;
+    grid = p.total_units;
+    if (a.order != kNaiveHeadFirst && grid > a.num_sms) grid = a.num_sms;
+    if (grid > 0x7fffffffLL) return -2;
+    dq_kernel<D><<<unsigned(grid), kThreads, CB::kSmemBytes, stream>>>(mq, mdo, mk, mv, p);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? 0 : note_cuda_error(e, "dq_kernel launch");
+}
+
+}  // namespace bwd
+
+int bwd_launch(const BwdLaunch &a, cudaStream_t stream) {
+    if (a.d <= 64) return bwd::launch<64>(a, stream);
+    return bwd::launch<128>(a, stream);
+}
+
+cudaError_t bwd_take_status(int *bits) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_bwd_status, sizeof(int));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(int));
+}
+
+}  // namespace attn

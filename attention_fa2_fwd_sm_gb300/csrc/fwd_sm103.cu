@@ -43,12 +43,15 @@ namespace attn {
 static __device__ int g_fwd_status;
 
 // Work counters of the persistent forward kernel: for each of kSchedSlots
-// launch slots, {next unit to hand out, CTAs finished}.  CTAs take units in
-// the chosen order by atomically incrementing `next`; the last CTA of the
-// launch to finish resets both to zero.  Successive launches rotate over the
-// slots, so launches only share a slot kSchedSlots launches apart.
+// launch slots, {next unit to hand out (die 0 in the die-split order), next
+// unit of die 1 (die-split order only), CTAs finished, unused}.  CTAs take
+// units in the chosen order by atomically incrementing a `next` counter; the
+// last CTA of the launch to finish resets the slot to zero.  Successive
+// launches rotate over the slots, so launches only share a slot kSchedSlots
+// launches apart.
 constexpr int kSchedSlots = 64;
-static __device__ unsigned int g_fwd_work[kSchedSlots][2];
+constexpr int kWorkDone = 2;
+static __device__ unsigned int g_fwd_work[kSchedSlots][4];
 
 namespace fwd {
 
@@ -90,11 +93,12 @@ struct Cfg {
 struct Params {
     __nv_bfloat16 *o;
     float *lse;
-    int N, Hq, Hkv, G, d_store, causal, order, nb;
+    int B, N, Hq, Hkv, G, d_store, causal, order, nb;
     long long total_units;
     float scale_log2;
     unsigned long long wait_ns;
     int sched_slot;  // g_fwd_work slot of this launch (persistent orders)
+    const int *die_of_sm;  // die of each SM id (die-split order; else null)
 };
 
 struct UnitWork {
@@ -128,9 +132,20 @@ __device__ __forceinline__ UnitWork unit_work(const Params &p, long long u) {
 // head-first: one unit per CTA, its block index.  Otherwise the next unit of
 // the order from the launch's work counter, so CTAs running at the same time
 // hold consecutive units (one ACC at a time in head-first order) and faster
-// CTAs simply take more units.
-__device__ __forceinline__ long long fetch_unit(const Params &p, long long i) {
+// CTAs simply take more units.  Die-split: each die has its own counter over
+// its own ACCs; a die whose ACCs are all handed out takes the other die's
+// remaining units, so no SM idles while work is left.
+__device__ __forceinline__ long long fetch_unit(const Params &p, long long i, int my_die) {
     if (p.order == kNaiveHeadFirst) return i == 0 ? (long long)blockIdx.x : -1;
+    if (p.order == kDieSplitHeadFirst) {
+        for (int s = 0; s < kDies; ++s) {
+            const int die = (my_die + s) % kDies;
+            const unsigned int k = atomicAdd(&g_fwd_work[p.sched_slot][die], 1u);
+            const long long u = die_split_unit(die, (long long)k, p.B, p.Hkv, p.G, p.nb);
+            if (u >= 0) return u;
+        }
+        return -1;
+    }
     const unsigned int u = atomicAdd(&g_fwd_work[p.sched_slot][0], 1u);
     return (long long)u < p.total_units ? (long long)u : -1;
 }
@@ -210,9 +225,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long fills = 0;          // K/V ring fills issued
             int q_loads[kNT] = {0, 0};    // Q loads issued per tile
             bool ok = true;
+            int my_die = 0;
+            if (p.die_of_sm) {
+                uint32_t smid;
+                asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+                if (smid < uint32_t(kDieMapMaxSms)) my_die = p.die_of_sm[smid] & 1;
+            }
             for (long long qi = 0; ok; ++qi) {
                 // Publish the next unit to the other roles (two-entry queue).
-                const long long u = fetch_unit(p, qi);
+                const long long u = fetch_unit(p, qi, my_die);
                 const int qs = int(qi & 1);
                 if (qi >= 2 && !mbar_wait_bounded(bar(C::kBarUQEmpty + qs), uint32_t(((qi >> 1) - 1) & 1),
                                                   p.wait_ns, abort_flag, status)) {
@@ -551,10 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Every CTA has fetched its last unit before it gets here, so the last
         // CTA to arrive may reset the launch's counters for the next user.
         __threadfence();
-        const unsigned int done = atomicAdd(&g_fwd_work[p.sched_slot][1], 1u);
+        const unsigned int done = atomicAdd(&g_fwd_work[p.sched_slot][kWorkDone], 1u);
         if (done == gridDim.x - 1) {
             atomicExch(&g_fwd_work[p.sched_slot][0], 0u);
             atomicExch(&g_fwd_work[p.sched_slot][1], 0u);
+            atomicExch(&g_fwd_work[p.sched_slot][kWorkDone], 0u);
         }
     }
 }
@@ -571,6 +593,7 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
     Params p;
     p.o = reinterpret_cast<__nv_bfloat16 *>(a.o);
     p.lse = a.lse;
+    p.B = a.B;
     p.N = a.N;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
@@ -584,6 +607,11 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
     p.wait_ns = a.wait_ns;
     static std::atomic<unsigned int> launch_seq{0};
     p.sched_slot = int(launch_seq.fetch_add(1) % kSchedSlots);
+    p.die_of_sm = nullptr;
+    if (a.order == kDieSplitHeadFirst) {
+        const int rc = die_map_device(&p.die_of_sm);
+        if (rc < 0) return rc;
+    }
     static bool attr_set = false;  // per instantiation; the attribute is per function
     if (!attr_set) {
         cudaFuncAttributes fa;

@@ -20,7 +20,9 @@ namespace attn {
 
 constexpr int kUnitRows = 256;  // query rows per unit (two 128-row MMA tiles)
 
-enum TileOrder : int { kHeadFirst = 0, kBlockFirst = 1, kNaiveHeadFirst = 2 };
+enum TileOrder : int { kHeadFirst = 0, kBlockFirst = 1, kNaiveHeadFirst = 2, kDieSplitHeadFirst = 3 };
+
+constexpr int kDies = 2;  // the GPU's two dies
 
 struct Tile {
     int b, h, m;  // batch entry, query head, 256-row block index
@@ -49,6 +51,30 @@ __host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int
     }
     t.m = causal ? (nb - 1 - r) : r;
     return t;
+}
+
+// Die-split head-first: the Attention Compute Clusters (ACC: the query heads
+// of one KV head of one batch entry, G * nb consecutive head-first units) are
+// dealt to the dies in turn, ACC a to die a % kDies, and each die walks its
+// own ACCs in head-first order.  This is the pages' Swizzled Head-first idea
+// (every ACC confined to one chiplet, detail page section 2 Q2 and Figure 10)
+// with the GPU's dies in place of XCDs.  Returns the head-first unit id of the
+// k-th unit of die `die`, or -1 when that die has no k-th unit.  (Unit ids are
+// head-first ids, so unit_to_tile maps them.)
+__host__ __device__ inline long long die_split_unit(int die, long long k, int B, int Hkv, int G, int nb) {
+    const long long upa = (long long)G * nb;  // units per ACC
+    const long long n_acc = (long long)B * Hkv;
+    if (k < 0 || die < 0 || die >= kDies) return -1;
+    const long long a = (k / upa) * kDies + die;  // ACC index
+    if (a >= n_acc) return -1;
+    return a * upa + (k % upa);
+}
+
+// Number of units die `die` owns under die-split head-first.
+__host__ __device__ inline long long die_split_units(int die, int B, int Hkv, int G, int nb) {
+    const long long n_acc = (long long)B * Hkv;
+    const long long accs = n_acc / kDies + (die < n_acc % kDies ? 1 : 0);
+    return accs * G * nb;
 }
 
 }  // namespace attn

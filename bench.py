@@ -284,7 +284,8 @@ def run_gpu(args):
             ms = e0.elapsed_time(e1) / reps
             abl[name] = {"ms": round(ms, 3), "tflops": round(flops / (ms / 1e3) / 1e12, 2)}
         result["ablation"] = abl
-        result["gpu_launches_ablation"] = 12
+        # 1 warm-up + 3 timed launches per order (plus the die map's one-off probe)
+        result["gpu_launches_ablation"] = 4 * len(attn.ORDERS)
 
     # -- end to end through the C ABI with host buffers --
     if args.e2e and rank == 0:
@@ -476,8 +477,8 @@ def run_decode_sweep(args):
 
 
 def run_fwd_sweep(args):
-    """Forward configurations of the pages' sweeps, each with the three tile
-    orders; one JSON line per configuration."""
+    """Forward configurations of the pages' sweeps, each with every tile
+    order; one JSON line per configuration."""
     import torch
 
     import attention_fa2_fwd_sm_gb300 as attn
@@ -519,18 +520,73 @@ def run_fwd_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_fwd_one(args):
+    """One forward configuration in one tile order: W warm-up launches, then K
+    timed launches (median); one JSON line.  Used for per-configuration
+    profiles (the sizes are flags)."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import prefill_inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    B, Hq, Hkv, N, d, causal = args.batch, args.hq, args.hkv, args.n, args.head_dim, args.causal
+    q, k, v = prefill_inputs(12, B, Hq, Hkv, N, d, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    oid = attn.ORDERS[args.order]
+    fn = lambda: attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, d ** -0.5, causal, oid,
+                                             stream.cuda_stream), "fwd")
+    for _ in range(args.warmup):
+        fn()
+    ms = _time_calls(torch, fn, args.steps, None, stream)
+    flops = fwd_flops(B, Hq, N, d, causal)
+    tf = flops / (ms / 1e3) / 1e12
+    print(json.dumps({"mode": "fwd-one", "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": causal,
+                      "order": args.order, "ms": round(ms, 4), "tflops": round(tf, 1),
+                      "frac": round(tf / peaks["bf16_tflops"], 4), "launches": args.warmup + args.steps}),
+          flush=True)
+
+
+def run_die_map(args):
+    """The SM -> die map the die-split order uses (measured on first use) with
+    its calibration statistics; one JSON line."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    _build.build()
+    torch.cuda.set_device(0)
+    dies, stats = attn.attn_die_map()
+    print(json.dumps({"mode": "die-map", "sms": len(dies), "die1_sms": sum(dies),
+                      "measured": stats[0] == 1.0, "min_margin": round(stats[1], 3),
+                      "near_clk": round(stats[2], 1), "far_clk": round(stats[3], 1),
+                      "die_of_sm": "".join(str(x) for x in dies)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--mode", default="step", choices=["step", "decode-sweep", "fwd-sweep"],
+    ap.add_argument("--mode", default="step",
+                    choices=["step", "decode-sweep", "fwd-sweep", "fwd-one", "die-map"],
                     help="step: the contract's one-line benchmark; the sweeps print one line "
-                         "per configuration")
+                         "per configuration; fwd-one times one forward configuration")
+    ap.add_argument("--batch", type=int, default=1, help="fwd-one: batch")
+    ap.add_argument("--hq", type=int, default=FWD["H"], help="fwd-one: query heads")
+    ap.add_argument("--hkv", type=int, default=FWD["H"], help="fwd-one: KV heads")
+    ap.add_argument("--head-dim", type=int, default=FWD["d"], help="fwd-one: head dimension")
+    ap.add_argument("--causal", action="store_true", help="fwd-one: causal mask")
     ap.add_argument("--n", type=int, default=FWD["N"], help="forward sequence length")
     ap.add_argument("--order", default="head_first", choices=["head_first", "block_first",
-                                                              "naive_head_first"])
+                                                              "naive_head_first",
+                                                              "die_split_head_first"])
     ap.add_argument("--no-ablation", dest="ablation", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
@@ -544,6 +600,10 @@ def main():
         return run_decode_sweep(args)
     if args.mode == "fwd-sweep":
         return run_fwd_sweep(args)
+    if args.mode == "fwd-one":
+        return run_fwd_one(args)
+    if args.mode == "die-map":
+        return run_die_map(args)
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)

@@ -62,11 +62,20 @@ enum attn_status {
  *  BLOCK_FIRST: all heads of one row block before the next row block (the
  *    pages' "Naive Block-first" baseline).
  *  NAIVE_HEAD_FIRST: head-first linear order, but one CTA per unit with the
- *    hardware choosing placement (the pages' "Naive Head-first"). */
+ *    hardware choosing placement (the pages' "Naive Head-first").
+ *  DIE_SPLIT_HEAD_FIRST: the pages' Swizzled Head-first with the GPU's two
+ *    dies in place of XCDs (detail page, section 2 Q2 and Figure 10): ACC a
+ *    (a = b * Hkv + KV head) belongs to die a % 2, the CTAs on each die walk
+ *    their die's ACCs in head-first order, and a die that runs out takes the
+ *    other die's remaining units.  Which SM is on which die is measured on the
+ *    first die-split launch on each device (see attn_die_map); that first
+ *    launch therefore synchronises the device and must not be captured into
+ *    a CUDA graph. */
 enum attn_tile_order {
     ATTN_ORDER_HEAD_FIRST = 0,
     ATTN_ORDER_BLOCK_FIRST = 1,
-    ATTN_ORDER_NAIVE_HEAD_FIRST = 2
+    ATTN_ORDER_NAIVE_HEAD_FIRST = 2,
+    ATTN_ORDER_DIE_SPLIT_HEAD_FIRST = 3
 };
 
 /*
@@ -91,6 +100,37 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
 int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
                 int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                 int tile_order, attn_stream_t stream);
+
+/*
+ * Backward pass of attn_fwd: gradients dQ, dK, dV for the output gradient
+ * dout.  The pages measure an FA2 backward pass under the same tile orders
+ * (detail page, section 5 "backward pass"); the gradient itself is the chain
+ * rule of the section-4 equation:
+ *   P = exp(scale * q k^T - lse),  dV = P^T dout,  dP = dout v^T,
+ *   Delta = rowsum(dout * o),  dS = P * (dP - Delta),
+ *   dQ = scale * dS k,  dK = scale * dS^T q,
+ * with the causal mask of the forward pass; for grouped-query attention the
+ * gradient of a KV head is the sum over the Hq / Hkv query heads that read it.
+ *   q, dout, o  [B, Hq,  N, d]  bf16 (o: the forward output)
+ *   k, v        [B, Hkv, N, d]  bf16
+ *   lse         [B, Hq,  N]     fp32, the forward's log-sum-exp (required)
+ *   dq          [B, Hq,  N, d]  bf16 (written)
+ *   dk, dv      [B, Hkv, N, d]  bf16 (written)
+ *   d in {56, 64, 128} as in attn_fwd; tile_order HEAD_FIRST, BLOCK_FIRST or
+ *   NAIVE_HEAD_FIRST (the die-split order is forward-only).
+ *   workspace: device memory of at least attn_bwd_workspace_bytes(B, Hq, N)
+ *   bytes, 16-byte aligned; it receives lse * log2(e) and Delta per query row.
+ * Three kernels run on `stream`: the Delta pre-pass, the dK/dV pass (one CTA
+ * per 128 keys of a KV head) and the dQ pass (one CTA per 128 query rows).
+ * Every output element is written once; results do not depend on the order.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+             const float *lse, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d,
+             float scale, int causal, int tile_order, void *workspace, size_t workspace_bytes,
+             attn_stream_t stream);
+
+/* Workspace bytes attn_bwd needs: 8 * B * Hq * roundup(N, 128) (0 for bad sizes). */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int N);
 
 /*
  * Split-KV grouped-query decode, one query row per (batch, query head).
@@ -178,9 +218,41 @@ int attn_decode_num_splits(int B, int Hq, int Hkv, int max_seqlen);
 
 /* Host-side view of the forward scheduler: unit `unit` of the order maps to
  * (*b, *h, *m) where m is the index of a 256-row block.  Pure host code; the
- * same function runs inside the kernel.  Returns ATTN_OK or ATTN_ERR_ARG. */
+ * same function runs inside the kernel.  Orders 0-2 only (the die-split order
+ * has one sequence per die: attn_tile_map_die_split).  Returns ATTN_OK or
+ * ATTN_ERR_ARG. */
 int attn_tile_map(int tile_order, int B, int Hq, int N, int causal, long long unit,
                   int *b, int *h, int *m);
+
+/* The k-th unit (k >= 0) that die `die` (0 or 1) takes from its own ACCs
+ * under ATTN_ORDER_DIE_SPLIT_HEAD_FIRST, as (*b, *h, *m).  Pure host code; the
+ * same function runs inside the kernel.  Returns ATTN_ERR_ARG when the die has
+ * no k-th unit (then its CTAs take the other die's remaining units). */
+int attn_tile_map_die_split(int B, int Hq, int Hkv, int N, int causal, int die, long long k,
+                            int *b, int *h, int *m);
+
+/* Which die each SM of the current device is on, as the die-split order uses
+ * it.  On the first call for a device (or the first die-split launch) a short
+ * calibration runs synchronously on the legacy default stream: one thread per
+ * SM times dependent L2 loads to 128 probe words (every address is homed in
+ * the L2 of one die, and far lines take longer), and the SMs are split into
+ * the two groups whose latency patterns agree (two-means on the correlation
+ * of the patterns; SM 0's group is die 0).  If the split is not clean (an SM
+ * correlates with its own group's mean pattern by less than 0.5 more than
+ * with the other group's, or a die would hold under a quarter of the SMs),
+ * SM ids are split in halves instead.  The map is kept for the life of the
+ * process; call this before any stream capture.
+ *   die_of_sm  host array of `capacity` ints, receives 0 or 1 for SM ids
+ *              0 .. min(capacity, SMs) - 1 (may be NULL when capacity is 0)
+ *   stats      host array of 4 floats (may be NULL): [0] 1 if measured, else
+ *              the reason for the halves fallback (0: the split was not
+ *              clean, -1: the probe did not reach every SM, -2: more SMs
+ *              than 256); [1] the smallest margin of an
+ *              SM (own-group minus other-group correlation, at most 2);
+ *              [2] / [3] mean near / far latency in SM clocks per dependent
+ *              L2 load.
+ * Returns the number of SMs, or a negative ATTN_ERR_* code. */
+int attn_die_map(int *die_of_sm, int capacity, float *stats);
 
 /* Number of work units (B * Hq * ceil(N / 256)) of the forward pass. */
 long long attn_fwd_units(int B, int Hq, int N);

@@ -17,6 +17,10 @@ Exploiting GPU Architectural NUMA Effects", section 2 Q2 and section 3
 * block-first: all heads of one row block before the next row block.
 * naive head-first: the head-first linear order, but each unit is its own
   CTA and the hardware decides where it runs.
+* die-split head-first: the pages' Swizzled Head-first placement (each ACC
+  confined to one chiplet, section 2 Q2 and Figure 10) with the GPU's two dies
+  in place of XCDs: ACCs are dealt to the dies in turn and each die takes its
+  own ACCs in head-first order (``die_split_sequence``).
 
 For causal attention the blocks of a head are visited last-block-first, so
 the longest units start first (the pages give only "ACC before next ACC";
@@ -77,3 +81,21 @@ def swizzle_chiplet(wgid: int, grid: int, num_xcd: int) -> int:
     """The chiplet swizzle baseline (detail page, section 7, Figure 3)."""
     per_xcd = grid // num_xcd
     return (wgid % num_xcd) * per_xcd + wgid // num_xcd
+
+
+def die_split_sequence(die: int, batch: int, hq: int, hkv: int, nb: int, causal: bool, dies: int = 2):
+    """Units of one die under die-split head-first, in the order that die
+    takes them.  The ACCs (batch entry b, KV head g; ACC index a = b*hkv + g)
+    are dealt round-robin, ACC a to die a % dies, and each die visits its ACCs
+    in increasing a, each ACC in head-first order: the ACC's query heads one
+    after the other, every row block of a head before the next head."""
+    g_size = hq // hkv
+    out = []
+    for a in range(batch * hkv):
+        if a % dies != die:
+            continue
+        b, kvh = divmod(a, hkv)
+        for h in range(kvh * g_size, (kvh + 1) * g_size):
+            for r in range(nb):
+                out.append((b, h, nb - 1 - r if causal else r))
+    return out

@@ -7,7 +7,8 @@ it without sharing any of the method.
 Recipe (the pages' workloads are Triton FA sweeps and Llama-3 / DeepSeek-V3
 shapes; no dataset is involved): every tensor is i.i.d. N(0, 1) drawn in fp32
 from a seeded ``torch.Generator`` and rounded to bf16 (round to nearest even).
-Seeds are ``1000 + cfg`` for Q, ``2000 + cfg`` for K and ``3000 + cfg`` for V.
+Seeds are ``1000 + cfg`` for Q, ``2000 + cfg`` for K, ``3000 + cfg`` for V and
+``4000 + cfg`` for the output gradient dO of the backward pass.
 Small cases draw on the CPU generator; large ones on the device generator of
 the tensor's device (deterministic for a given device and seed).
 """
@@ -17,7 +18,7 @@ import math
 
 import torch
 
-SEED_Q, SEED_K, SEED_V = 1000, 2000, 3000
+SEED_Q, SEED_K, SEED_V, SEED_DO = 1000, 2000, 3000, 4000
 
 
 def normal_bf16(shape, seed: int, device="cpu") -> torch.Tensor:
@@ -37,6 +38,11 @@ def prefill_inputs(cfg: int, B: int, Hq: int, Hkv: int, N: int, d: int, device="
     k = normal_bf16((B, Hkv, N, d), SEED_K + cfg, device)
     v = normal_bf16((B, Hkv, N, d), SEED_V + cfg, device)
     return q, k, v
+
+
+def output_grad(cfg: int, B: int, Hq: int, N: int, d: int, device="cpu"):
+    """dO ``[B, Hq, N, d]`` bf16 (the backward pass's incoming gradient)."""
+    return normal_bf16((B, Hq, N, d), SEED_DO + cfg, device)
 
 
 def decode_inputs(cfg: int, B: int, Hq: int, Hkv: int, s_max: int, d: int, device="cpu"):

@@ -65,6 +65,24 @@ def test_scheduler_rejects_bad_units(L):
         attn.attn_tile_map(7, 1, 2, 256, False, 0)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,N", [(1, 8, 8, 300), (1, 64, 8, 1024), (3, 6, 3, 257), (1, 4, 1, 256)])
+def test_die_split_scheduler_matches_the_definition(L, causal, B, Hq, Hkv, N):
+    nb = T.num_blocks(N, 256)
+    for die in (0, 1):
+        want = T.die_split_sequence(die, B, Hq, Hkv, nb, causal)
+        got = [attn.attn_tile_map_die_split(B, Hq, Hkv, N, causal, die, k) for k in range(len(want))]
+        assert got == want
+        assert attn.attn_tile_map_die_split(B, Hq, Hkv, N, causal, die, len(want)) is None
+
+
+def test_tile_map_rejects_the_die_split_order(L):
+    with pytest.raises(attn.AttnError):
+        attn.attn_tile_map(3, 1, 2, 256, False, 0)
+    assert attn.attn_tile_map_die_split(1, 2, 2, 256, False, 2, 0) is None  # no die 2
+    assert attn.attn_tile_map_die_split(1, 2, 2, 256, False, 0, -1) is None
+
+
 def _fwd(**kw):
     a = dict(q=A16, k=A16, v=A16, o=A16, lse=None, B=1, Hq=2, Hkv=2, N=256, d=64, scale=0.125,
              causal=False, tile_order=0, stream=0)
@@ -82,7 +100,8 @@ def _fwd(**kw):
     (dict(Hq=3, Hkv=2), attn.ATTN_ERR_ARG),
     (dict(scale=0.0), attn.ATTN_ERR_ARG),
     (dict(scale=float("nan")), attn.ATTN_ERR_ARG),
-    (dict(tile_order=3), attn.ATTN_ERR_ARG),
+    (dict(tile_order=4), attn.ATTN_ERR_ARG),
+    (dict(tile_order=-1), attn.ATTN_ERR_ARG),
     (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
     (dict(d=32), attn.ATTN_ERR_UNSUPPORTED),
     (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
@@ -142,3 +161,36 @@ def test_noalloc_decode_refuses_on_the_host(L):
     assert attn.attn_decode_noalloc(None, *p[1:], 2, 64, 8, 128, 0.1, 4, 1024, 0) == attn.ATTN_ERR_ARG
     assert attn.attn_decode_noalloc(*p, 2, 64, 8, 56, 0.1, 4, 1024, 0) == attn.ATTN_ERR_UNSUPPORTED
     assert attn.attn_decode_noalloc(*p, 2, 64, 8, 128, 0.1, 300, 1024, 0) == attn.ATTN_ERR_ARG
+
+
+def _bwd(**kw):
+    a = dict(q=A16, k=A16, v=A16, o=A16, dout=A16, lse=A16, dq=A16, dk=A16, dv=A16, B=1, Hq=2, Hkv=2, N=256,
+             d=64, scale=0.125, causal=False, order=0, ws=A16, ws_bytes=1 << 20, stream=0)
+    a.update(kw)
+    return attn.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"],
+                         a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], a["scale"], a["causal"], a["order"],
+                         a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_ARG),
+    (dict(dout=A16 + 2), attn.ATTN_ERR_ARG),
+    (dict(lse=None), attn.ATTN_ERR_ARG),
+    (dict(lse=A16 + 2), attn.ATTN_ERR_ARG),
+    (dict(dk=None), attn.ATTN_ERR_ARG),
+    (dict(Hq=3, Hkv=2), attn.ATTN_ERR_ARG),
+    (dict(scale=-1.0), attn.ATTN_ERR_ARG),
+    (dict(order=3), attn.ATTN_ERR_ARG),
+    (dict(d=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(ws=None), attn.ATTN_ERR_WORKSPACE),
+    (dict(ws=A16 + 4), attn.ATTN_ERR_WORKSPACE),
+    (dict(ws_bytes=2 * 2 * 256 * 4 - 1), attn.ATTN_ERR_WORKSPACE),
+])
+def test_backward_argument_errors(L, kw, code):
+    assert _bwd(**kw) == code
+
+
+def test_backward_workspace_size(L):
+    assert attn.attn_bwd_workspace_bytes(1, 2, 256) == 2 * 2 * 256 * 4
+    assert attn.attn_bwd_workspace_bytes(2, 3, 129) == 2 * 2 * 3 * 256 * 4  # rows padded to 128
+    assert attn.attn_bwd_workspace_bytes(0, 2, 256) == 0

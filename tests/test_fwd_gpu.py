@@ -3,7 +3,7 @@
 Small shapes are compared element by element (several tiles, ragged tails,
 N = 1, GQA, causal, d = 56/64/128); the full sizes of the benchmark
 configurations are compared on sampled rows of sampled heads.  Structural
-identities are checked bit for bit: the three tile orders, GQA against MHA
+identities are checked bit for bit: the four tile orders, GQA against MHA
 with repeated K/V, and d = 56 against explicit zero padding to 64."""
 import gc
 
@@ -70,7 +70,7 @@ def test_tile_orders_are_bit_identical_and_correct(attn, causal):
     dev = torch.device("cuda")
     B, Hq, Hkv, N, d = 1, 64, 8, 2048 + 77, 128
     q, k, v = prefill_inputs(2, B, Hq, Hkv, N, d, dev)
-    outs = [_run(attn, q, k, v, causal, order=o) for o in (0, 1, 2)]
+    outs = [_run(attn, q, k, v, causal, order=o) for o in (0, 1, 2, 3)]
     for o, lse in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
     o, lse = outs[0]
@@ -81,6 +81,30 @@ def test_tile_orders_are_bit_identical_and_correct(attn, causal):
         o_ref, l_ref = oracle.attention_rows(to64(q[0, h, rows]), to64(k[0, g]), to64(v[0, g]), scale,
                                              causal, rows)
         assert_close(to64(o[0, h, rows]), o_ref, to64(lse[0, h, rows]), l_ref, what=f"head {h}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_die_split_order_with_an_odd_acc_count(attn, causal):
+    """Nine ACCs over two dies (one die runs out first and takes the other's
+    units); the result is bit-identical to head-first and matches the oracle."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N, d = 3, 6, 3, 1000, 64
+    q, k, v = prefill_inputs(4, B, Hq, Hkv, N, d, dev)
+    o0, l0 = _run(attn, q, k, v, causal, order=0)
+    o3, l3 = _run(attn, q, k, v, causal, order=3)
+    assert torch.equal(o0, o3) and torch.equal(l0, l3)
+    o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), scale_of(d), causal)
+    assert_close(to64(o3), o_ref, to64(l3), lse_ref, what="die split")
+
+
+def test_die_map_is_a_two_way_partition(attn):
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    dies, stats = attn.attn_die_map()
+    assert len(dies) == n and set(dies) <= {0, 1} and dies[0] == 0
+    assert n // 4 <= sum(dies) <= n - n // 4
+    if stats[0] == 1.0:  # measured: clean split, far loads slower than near ones
+        assert stats[1] >= 0.5 and stats[3] > stats[2] > 0
+    assert attn.attn_die_map() == (dies, stats)  # measured once per device
 
 
 def test_d56_equals_zero_padding_to_64(attn):

@@ -100,3 +100,30 @@ def test_swizzle_rejects_heads_not_divisible_by_xcds():
 def test_chiplet_swizzle_is_a_permutation():
     for X, grid in [(8, 64), (4, 4096)]:
         assert sorted(T.swizzle_chiplet(w, grid, X) for w in range(grid)) == list(range(grid))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,nb", [(1, 128, 128, 4), (1, 64, 8, 3), (3, 8, 1, 2), (2, 6, 3, 5)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_die_split_partitions_units_by_acc(B, Hq, Hkv, nb, causal):
+    seqs = [T.die_split_sequence(d, B, Hq, Hkv, nb, causal) for d in (0, 1)]
+    every = [x for s in seqs for x in s]
+    assert sorted(every) == sorted((b, h, m) for b in range(B) for h in range(Hq) for m in range(nb))
+    G = Hq // Hkv
+    for d, seq in enumerate(seqs):  # each ACC lives on exactly one die
+        assert all(((b * Hkv + h // G) % 2) == d for b, h, _ in seq)
+
+
+def test_die_split_each_die_is_head_first_over_its_accs():
+    """Per die the order is the head-first order restricted to that die's
+    ACCs; for one ACC per die it is exactly the head-first order of that ACC."""
+    B, Hq, Hkv, nb = 1, 4, 2, 3
+    hf = [T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, True) for u in range(B * Hq * nb)]
+    G = Hq // Hkv
+    for d in (0, 1):
+        assert T.die_split_sequence(d, B, Hq, Hkv, nb, True) == [x for x in hf if x[1] // G == d]
+
+
+def test_die_split_with_one_die_is_head_first():
+    B, Hq, Hkv, nb = 2, 6, 3, 4
+    assert T.die_split_sequence(0, B, Hq, Hkv, nb, False, dies=1) == [
+        T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, False) for u in range(B * Hq * nb)]
