@@ -46,6 +46,8 @@ SIGNATURES = {
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "attn_decode_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    "attn_decode_varlen_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "attn_tile_map": (_I, [_I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
     "attn_tile_map_die_split": (_I, [_I, _I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
@@ -150,6 +152,34 @@ def attn_decode_noalloc(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, num
 
 
 DECODE_NOALLOC_SCRATCH_BYTES = 4194304
+
+
+def attn_decode_varlen(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, max_seqlen, workspace,
+                       workspace_bytes, stream=None) -> int:
+    return lib().attn_decode_varlen(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(o), B, Hq, Hkv,
+                                    d, float(scale), int(max_seqlen), _ptr(workspace), int(workspace_bytes),
+                                    _stream(stream))
+
+
+def attn_decode_varlen_workspace_bytes(B, Hq, Hkv, d) -> int:
+    return int(lib().attn_decode_varlen_workspace_bytes(B, Hq, Hkv, d))
+
+
+def decode_varlen(q, kcache, vcache, seqlens, scale=None, workspace=None, stream=None):
+    """Allocate the output (and a workspace when none is given) and run
+    attn_decode_varlen; returns ``(o, workspace)``."""
+    import torch
+    B, Hq, d = q.shape
+    Hkv, s_max = kcache.shape[1], kcache.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    nbytes = attn_decode_varlen_workspace_bytes(B, Hq, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    check(attn_decode_varlen(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, s_max, workspace,
+                             workspace.numel(), stream), "attn_decode_varlen")
+    return o, workspace
 
 
 def attn_decode_workspace_bytes(B, Hq, d, num_splits) -> int:

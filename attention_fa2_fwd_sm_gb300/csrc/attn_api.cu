@@ -264,6 +264,78 @@ int attn_decode_num_splits(int B, int Hq, int Hkv, int max_seqlen) {
     return splits_for(B, Hkv, max_seqlen, sms);
 }
 
+// Varlen decode: work-list capacity and the chunk rule (see attn.h).
+constexpr int kVarlenMinChunk = 512;
+static long long varlen_target(int sms) {
+    const long long t = (5LL * sms) / 3;
+    return t > 0 ? t : 1;
+}
+static long long varlen_max_items(int B, int Hkv, int sms) {
+    const long long t = varlen_target(sms);
+    return (t + Hkv - 1) / Hkv + B;
+}
+static void varlen_layout(int B, int Hq, int d, long long items, size_t *plan_bytes, size_t *o_bytes,
+                          size_t *lse_bytes) {
+    *plan_bytes = ((size_t)(2 + 2LL * B + 3 * items) * sizeof(int) + 255) / 256 * 256;
+    *o_bytes = ((size_t)items * Hq * d * sizeof(float) + 255) / 256 * 256;
+    *lse_bytes = (size_t)items * Hq * sizeof(float);
+}
+
+size_t attn_decode_varlen_workspace_bytes(int B, int Hq, int Hkv, int d) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv) return 0;
+    const int sms = current_num_sms();
+    if (sms <= 0) return 0;
+    size_t a, b, c;
+    varlen_layout(B, Hq, d, varlen_max_items(B, Hkv, sms), &a, &b, &c);
+    return a + b + c;
+}
+
+int attn_decode_varlen(const void *q, const void *kcache, const void *vcache, const int *seqlens, void *o,
+                       int B, int Hq, int Hkv, int d, float scale, int max_seqlen, void *workspace,
+                       size_t workspace_bytes, attn_stream_t stream) {
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) || !seqlens ||
+        (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+        return ATTN_ERR_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || max_seqlen <= 0 || Hq % Hkv) return ATTN_ERR_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (Hq / Hkv > kDecodeMaxGroup) return ATTN_ERR_UNSUPPORTED;
+    if (B > (1 << 20) || Hkv > 65535 || (long long)max_seqlen * d * 2 >= (1LL << 39)) return ATTN_ERR_ARG;
+    // the plan's T * Hkv stays below 2^62; the merge grid has B * Hq blocks
+    if ((double)B * (double)max_seqlen * (double)Hkv >= 4.0e18 || (long long)B * Hq > 0x7fffffffLL)
+        return ATTN_ERR_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 15u)) return ATTN_ERR_WORKSPACE;
+    const int sms = current_num_sms();
+    if (sms <= 0) return note_cuda_error(cudaErrorNoDevice, "device query");
+    const long long items = varlen_max_items(B, Hkv, sms);
+    if (items > 65535) return ATTN_ERR_ARG;  // grid.y limit of the decode launch
+    size_t plan_bytes, o_bytes, lse_bytes;
+    varlen_layout(B, Hq, d, items, &plan_bytes, &o_bytes, &lse_bytes);
+    if (workspace_bytes < plan_bytes + o_bytes + lse_bytes) return ATTN_ERR_WORKSPACE;
+    DecodeLaunch a;
+    a.q = q;
+    a.kcache = kcache;
+    a.vcache = vcache;
+    a.seqlens = seqlens;
+    a.o = o;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.max_seqlen = max_seqlen;
+    a.num_splits = 0;
+    a.scale = scale;
+    char *ws = static_cast<char *>(workspace);
+    a.plan = reinterpret_cast<int *>(ws);
+    a.ws_o = reinterpret_cast<float *>(ws + plan_bytes);
+    a.ws_lse = reinterpret_cast<float *>(ws + plan_bytes + o_bytes);
+    a.varlen_max_items = int(items);
+    a.varlen_target = varlen_target(sms);
+    a.varlen_min_chunk = kVarlenMinChunk;
+    a.wait_ns = (unsigned long long)g_wait_ns.load();
+    return decode_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int attn_decode(const void *q, const void *kcache, const void *vcache, const int *seqlens, void *o,
                 int B, int Hq, int Hkv, int d, float scale, int num_splits, int max_seqlen,
                 void *workspace, size_t workspace_bytes, attn_stream_t stream) {

@@ -40,6 +40,11 @@ struct DecodeLaunch {
     float scale;
     float *ws_o, *ws_lse;  // partial outputs / log-sum-exps (used when splits > 1)
     unsigned long long wait_ns;
+    // Varlen path (plan != null): work list, its capacity, and the chunk rule.
+    int *plan = nullptr;
+    int varlen_max_items = 0;
+    long long varlen_target = 0;
+    int varlen_min_chunk = 0;
 };
 
 // Record a failed CUDA call for attn_last_error() (this thread) and return

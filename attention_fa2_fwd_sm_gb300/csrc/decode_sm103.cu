@@ -18,6 +18,16 @@
 // end the four warp states are combined through shared memory into the
 // split's partial (O_s normalised, lse_s), or into O directly when there is a
 // single split.
+//
+// Ragged multi-user batches (attn_decode_varlen): one chunk size for the whole
+// batch, chosen on the device from the total number of cached keys, cuts every
+// sequence into chunks; a plan kernel writes the resulting work list (batch
+// entry, key range) and each decode CTA takes one item of it, so a long
+// sequence is spread over many CTAs however short the others are.  The
+// reduction then has two levels, as in the kernbench2 decode family's
+// multi-user "two-level reduce-to-root" (short-context section): the warps of
+// a CTA are combined in shared memory, and one merge per (user, query head)
+// reduces that user's chunks.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -66,10 +76,16 @@ struct Params {
     const int *seqlens;
     __nv_bfloat16 *o;
     float *ws_o, *ws_lse;
-    int Hq, Hkv, G, max_seqlen, num_splits;
+    const int *plan;  // work list of the varlen path (null: split grid)
+    int B, Hq, Hkv, G, max_seqlen, num_splits;
     float scale_log2;
     unsigned long long wait_ns;
 };
+
+// Varlen plan layout (ints): [0] item count, [1] chunk size C, [2, 2 + B)
+// first item of each batch entry, [2 + B, 2 + 2B) its item count, then the
+// items as (b, lo, hi) triples.
+__host__ __device__ inline int plan_items_offset(int B) { return 2 + 2 * B; }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                                uint32_t b1) {
@@ -120,15 +136,30 @@ __global__ void __launch_bounds__(kThreads)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + C::kNumBars);
     int *status = &g_decode_status;
 
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // Varlen grid: (KV head, work item), so the KV heads of one sequence are
+    // launched together as in the split grid (split, KV head, batch).
+    const int split = p.plan ? blockIdx.y : blockIdx.x;
+    const int g = p.plan ? blockIdx.x : blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    int seqlen = p.seqlens[b];
-    seqlen = seqlen < 0 ? 0 : (seqlen > p.max_seqlen ? p.max_seqlen : seqlen);
-    int per = (seqlen + p.num_splits - 1) / p.num_splits;
-    const int chunk = (per + kChunkGranule - 1) / kChunkGranule * kChunkGranule;
-    const int lo = min(split * chunk, seqlen);
-    const int hi = min(lo + chunk, seqlen);
+    int b, lo, hi;
+    if (p.plan) {
+        // Varlen: this CTA is work item `split` of the plan (the grid is an
+        // upper bound on the item count; CTAs past it have nothing to do).
+        if (split >= p.plan[0]) return;
+        const int *it = p.plan + plan_items_offset(p.B) + 3 * split;
+        b = it[0];
+        lo = it[1];
+        hi = it[2];
+    } else {
+        b = blockIdx.z;
+        int seqlen = p.seqlens[b];
+        seqlen = seqlen < 0 ? 0 : (seqlen > p.max_seqlen ? p.max_seqlen : seqlen);
+        int per = (seqlen + p.num_splits - 1) / p.num_splits;
+        const int chunk = (per + kChunkGranule - 1) / kChunkGranule * kChunkGranule;
+        lo = min(split * chunk, seqlen);
+        hi = min(lo + chunk, seqlen);
+    }
     const int ntiles = (hi - lo + kKeysPerStage - 1) / kKeysPerStage;
 
     if (threadIdx.x == 0) {
@@ -336,7 +367,11 @@ __global__ void __launch_bounds__(kThreads)
         }
         const float o = wsum > 0.f ? osum / wsum : 0.f;
         const int h = g * G + row;
-        if (p.num_splits == 1) {
+        if (p.plan) {
+            const size_t pi = (size_t)split * p.Hq + h;
+            p.ws_o[pi * D + col] = o;
+            if (col == 0) p.ws_lse[pi] = wsum > 0.f ? (M + __log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+        } else if (p.num_splits == 1) {
             p.o[(size_t)(b * p.Hq + h) * D + col] = __float2bfloat16_rn(o);
         } else {
             const size_t pi = (size_t)(b * p.Hq + h) * p.num_splits + split;
@@ -366,6 +401,95 @@ __global__ void __launch_bounds__(D) merge_kernel(const float *ws_o, const float
     o[(size_t)bh * D + col] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
 }
 
+// Varlen plan, one CTA: total keys T = sum_b min(max(seqlens[b], 0), max_seqlen);
+// chunk C = max(min_chunk, ceil(T * Hkv / target) rounded up to 64); sequence
+// b gets n_b = ceil(len_b / C) items [c C, min(c C + C, len_b)), numbered
+// consecutively by b.  The item count is at most ceil(target / Hkv) + B.
+__global__ void __launch_bounds__(256) varlen_plan_kernel(const int *seqlens, int B, int max_seqlen, int Hkv,
+                                                          long long target, int min_chunk, int *plan) {
+    __shared__ long long warp_part[8];
+    __shared__ int chunk_s;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int per = (B + 255) / 256;  // consecutive sequences per thread
+    const int b0 = min(t * per, B), b1 = min(b0 + per, B);
+    auto len_of = [&](int b) {
+        const int n = seqlens[b];
+        return n < 0 ? 0 : (n > max_seqlen ? max_seqlen : n);
+    };
+    // Inclusive block scan of one value per thread (warp shuffles, then the
+    // eight warp totals); returns the thread's exclusive prefix and the total.
+    auto block_scan = [&](long long v, long long &total) {
+        long long x = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        __syncthreads();
+        if (lane == 31) warp_part[w] = x;
+        __syncthreads();
+        long long before = 0;
+        total = 0;
+        for (int i = 0; i < 8; ++i) {
+            if (i < w) before += warp_part[i];
+            total += warp_part[i];
+        }
+        return before + x - v;
+    };
+    long long keys = 0;
+    for (int b = b0; b < b1; ++b) keys += len_of(b);
+    long long T = 0;
+    block_scan(keys, T);
+    if (t == 0) {
+        long long c = (T * Hkv + target - 1) / target;
+        c = (c + kChunkGranule - 1) / kChunkGranule * kChunkGranule;
+        if (c < min_chunk) c = min_chunk;
+        chunk_s = int(c < 0x40000000LL ? c : 0x40000000LL);
+        plan[1] = chunk_s;
+    }
+    __syncthreads();
+    const int C = chunk_s;
+    long long mine = 0;  // items of this thread's sequences
+    for (int b = b0; b < b1; ++b) mine += (len_of(b) + C - 1) / C;
+    long long count = 0;
+    int first = int(block_scan(mine, count));
+    if (t == 0) plan[0] = int(count);
+    int *items = plan + plan_items_offset(B);
+    for (int b = b0; b < b1; ++b) {
+        const int len = len_of(b);
+        const int n = (len + C - 1) / C;
+        plan[2 + b] = first;
+        plan[2 + B + b] = n;
+        for (int c = 0; c < n; ++c) {
+            int *it = items + 3 * (first + c);
+            it[0] = b;
+            it[1] = c * C;
+            it[2] = min(c * C + C, len);
+        }
+        first += n;
+    }
+}
+
+// Varlen merge: for (b, h), the n_b partials of b's items.  n_b = 0 gives O = 0.
+template <int D>
+__global__ void __launch_bounds__(D) merge_varlen_kernel(const int *plan, int B, int Hq, const float *ws_o,
+                                                         const float *ws_lse, __nv_bfloat16 *o) {
+    const int bh = blockIdx.x, col = threadIdx.x;
+    const int b = bh / Hq, h = bh % Hq;
+    const int f = plan[2 + b], n = plan[2 + B + b];
+    float L = -INFINITY;
+    for (int s = f; s < f + n; ++s) L = fmaxf(L, ws_lse[(size_t)s * Hq + h]);
+    float wsum = 0.f, acc = 0.f;
+    if (L != -INFINITY) {
+        for (int s = f; s < f + n; ++s) {
+            const float w = __expf(ws_lse[(size_t)s * Hq + h] - L);
+            wsum += w;
+            acc += w * ws_o[((size_t)s * Hq + h) * D + col];
+        }
+    }
+    o[(size_t)bh * D + col] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+}
+
 template <int D>
 int launch(const DecodeLaunch &a, cudaStream_t stream) {
     using C = Cfg<D>;
@@ -381,6 +505,8 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
     p.o = reinterpret_cast<__nv_bfloat16 *>(a.o);
     p.ws_o = a.ws_o;
     p.ws_lse = a.ws_lse;
+    p.plan = a.plan;
+    p.B = a.B;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.G = a.Hq / a.Hkv;
@@ -394,6 +520,18 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
             decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(decode_kernel)");
         attr_set = true;
+    }
+    if (a.plan) {
+        varlen_plan_kernel<<<1, 256, 0, stream>>>(a.seqlens, a.B, a.max_seqlen, a.Hkv, a.varlen_target,
+                                                  a.varlen_min_chunk, a.plan);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return note_cuda_error(e, "varlen_plan_kernel launch");
+        decode_kernel<D><<<dim3(a.Hkv, a.varlen_max_items, 1), dim3(kThreads), C::kSmemBytes, stream>>>(mk, mv, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return note_cuda_error(e, "decode_kernel launch (varlen)");
+        merge_varlen_kernel<D><<<dim3(a.B * a.Hq), dim3(D), 0, stream>>>(a.plan, a.B, a.Hq, a.ws_o, a.ws_lse, p.o);
+        e = cudaGetLastError();
+        return e == cudaSuccess ? 0 : note_cuda_error(e, "merge_varlen_kernel launch");
     }
     decode_kernel<D><<<dim3(a.num_splits, a.Hkv, a.B), dim3(kThreads), C::kSmemBytes, stream>>>(mk, mv, p);
     cudaError_t e = cudaGetLastError();

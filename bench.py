@@ -552,6 +552,100 @@ def run_fwd_one(args):
           flush=True)
 
 
+def bwd_flops(B, H, N, d, causal):
+    """Algorithmic backward work: five products of 2*N*N*d per head (dV, dP,
+    dK, dQ and the recomputed S), half of that causal."""
+    f = 10.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def run_bwd_one(args):
+    """The backward pass of one configuration in one tile order: W warm-up
+    calls, then K timed calls (median); one JSON line."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import output_grad, prefill_inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    B, Hq, Hkv, N, d, causal = args.batch, args.hq, args.hkv, args.n, args.head_dim, args.causal
+    if args.order not in ("head_first", "block_first", "naive_head_first"):
+        raise SystemExit("the backward pass takes head_first, block_first or naive_head_first")
+    q, k, v = prefill_inputs(13, B, Hq, Hkv, N, d, dev)
+    dout = output_grad(13, B, Hq, N, d, dev)
+    o, lse = attn.forward(q, k, v, causal=causal, scale=d ** -0.5)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = attn.attn_bwd_workspace_bytes(B, Hq, N)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    oid = attn.ORDERS[args.order]
+    fn = lambda: attn.check(attn.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, d ** -0.5,
+                                          causal, oid, ws, nbytes, stream.cuda_stream), "bwd")
+    for _ in range(args.warmup):
+        fn()
+    ms = _time_calls(torch, fn, args.steps, None, stream)
+    tf = bwd_flops(B, Hq, N, d, causal) / (ms / 1e3) / 1e12
+    print(json.dumps({"mode": "bwd-one", "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": causal,
+                      "order": args.order, "ms": round(ms, 4), "tflops": round(tf, 1),
+                      "frac": round(tf / peaks["bf16_tflops"], 4),
+                      "launches_per_call": 3, "calls": args.warmup + args.steps}), flush=True)
+
+
+def run_decode_varlen(args):
+    """Ragged multi-user decode batches (GQA Hq=64, Hkv=8, d=128): attn_decode
+    (split count from max_seqlen) against attn_decode_varlen (chunks from the
+    total attended keys).  GB/s counts the attended K/V bytes plus q and o."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import decode_inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    Hq, Hkv, d = 64, 8, 128
+    g = torch.Generator().manual_seed(77)
+    workloads = [
+        ("one 64K user + 15 users of 2K", 65536, [65536] + [2048] * 15),
+        ("64 users, lengths uniform in [1, 16K]", 16384, torch.randint(1, 16385, (64,), generator=g).tolist()),
+        ("8 users of 32K (equal lengths)", 32768, [32768] * 8),
+    ]
+    for name, s_max, lens in workloads:
+        B = len(lens)
+        q, kc, vc = decode_inputs(14, B, Hq, Hkv, s_max, d, dev)
+        seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        nbytes = sum(lens) * Hkv * d * 2 * 2 + 2 * B * Hq * d * 2
+        splits = attn.attn_decode_num_splits(B, Hq, Hkv, s_max)
+        ws_s = torch.empty(max(attn.attn_decode_workspace_bytes(B, Hq, d, splits), 16), dtype=torch.uint8,
+                           device=dev)
+        ws_v = torch.empty(max(attn.attn_decode_varlen_workspace_bytes(B, Hq, Hkv, d), 16), dtype=torch.uint8,
+                           device=dev)
+        split_fn = lambda: attn.check(attn.attn_decode(q, kc, vc, seq, o, B, Hq, Hkv, d, d ** -0.5, splits, s_max,
+                                                       ws_s, ws_s.numel(), stream.cuda_stream), "decode")
+        varlen_fn = lambda: attn.check(attn.attn_decode_varlen(q, kc, vc, seq, o, B, Hq, Hkv, d, d ** -0.5, s_max,
+                                                               ws_v, ws_v.numel(), stream.cuda_stream), "varlen")
+        out = {"mode": "decode-varlen", "workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d,
+               "attended_keys": sum(lens), "bytes": nbytes}
+        for key, fn in (("split", split_fn), ("varlen", varlen_fn)):
+            for _ in range(args.warmup):
+                fn()
+            us = _time_calls(torch, fn, args.steps, None, stream) * 1e3
+            gbs = nbytes / (us * 1e-6) / 1e9
+            out[key] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        out["split"]["splits"] = splits
+        out["varlen"]["chunk"] = int(ws_v[4:8].view(torch.int32).item())
+        out["varlen"]["chunks"] = int(ws_v[0:4].view(torch.int32).item())
+        print(json.dumps(out), flush=True)
+        del q, kc, vc
+        torch.cuda.empty_cache()
+
+
 def run_die_map(args):
     """The SM -> die map the die-split order uses (measured on first use) with
     its calibration statistics; one JSON line."""
@@ -575,7 +669,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--mode", default="step",
-                    choices=["step", "decode-sweep", "fwd-sweep", "fwd-one", "die-map"],
+                    choices=["step", "decode-sweep", "decode-varlen", "fwd-sweep", "fwd-one", "bwd-one",
+                             "die-map"],
                     help="step: the contract's one-line benchmark; the sweeps print one line "
                          "per configuration; fwd-one times one forward configuration")
     ap.add_argument("--batch", type=int, default=1, help="fwd-one: batch")
@@ -604,6 +699,10 @@ def main():
         return run_fwd_one(args)
     if args.mode == "die-map":
         return run_die_map(args)
+    if args.mode == "bwd-one":
+        return run_bwd_one(args)
+    if args.mode == "decode-varlen":
+        return run_decode_varlen(args)
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)

@@ -205,6 +205,38 @@ int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache,
                         const int *seqlens, void *o, int B, int Hq, int Hkv, int d,
                         float scale, int num_splits, int max_seqlen, attn_stream_t stream);
 
+/*
+ * Decode for a ragged multi-user batch: the same computation and layouts as
+ * attn_decode, with the work balanced over the whole batch instead of a fixed
+ * split count per sequence.  kernbench2 "Fused Grouped-Query Attention":
+ * the decode family reduces partial outputs per user in two levels
+ * ("two-level reduce-to-root", short-context section); here the levels are
+ * the warps of a CTA (combined in shared memory) and the chunks of a user
+ * (one merge per (user, query head)).
+ * Three kernels run on `stream`, with no host synchronisation:
+ *   1. a one-CTA plan: T = sum_b min(max(seqlens[b], 0), max_seqlen) keys in
+ *      all; chunk C = max(512, ceil(T * Hkv / target) rounded up to 64) with
+ *      target = floor(5 * SMs / 3) (at least 1); sequence b is cut into
+ *      n_b = ceil(len_b / C) chunks [c C, min(c C + C, len_b)), numbered
+ *      consecutively in b;
+ *   2. one decode CTA per (chunk, KV head);
+ *   3. the merge of each (b, query head) over b's chunks (O = 0 when n_b = 0).
+ * workspace: at least attn_decode_varlen_workspace_bytes(B, Hq, Hkv, d)
+ * bytes, 16-byte aligned.  Its head holds the plan as int32: [0] chunk
+ * count, [1] C, [2, 2 + B) first chunk of each b, [2 + B, 2 + 2B) n_b, then
+ * (b, lo, hi) per chunk; the partial states follow.  Arguments and errors as
+ * attn_decode (no num_splits); d in {64, 128}, Hq / Hkv <= 16, and
+ * ceil(target / Hkv) + B <= 65535.
+ */
+int attn_decode_varlen(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                       void *o, int B, int Hq, int Hkv, int d, float scale, int max_seqlen,
+                       void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/* Workspace bytes attn_decode_varlen needs on the current device: room for
+ * ceil(target / Hkv) + B chunks (the most the plan can make), with target as
+ * above.  0 for bad sizes or when the device cannot be queried. */
+size_t attn_decode_varlen_workspace_bytes(int B, int Hq, int Hkv, int d);
+
 /* Bytes of workspace attn_decode needs for this shape and split count
  * (0 when num_splits == 1).  num_splits <= 0 is not resolved here: pass the
  * value returned by attn_decode_num_splits. */

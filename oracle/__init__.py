@@ -217,6 +217,27 @@ def split_ranges(seqlen: int, num_splits: int, granule: int = 64):
     return out
 
 
+def varlen_plan(seqlens, max_seqlen: int, hkv: int, target: int, min_chunk: int = 512, granule: int = 64):
+    """Work list of the ragged multi-user decode (integer arithmetic): one chunk
+    size for the whole batch, C = max(min_chunk, ceil(T * hkv / target) rounded
+    up to ``granule``) with T the total number of attended keys; sequence b is
+    cut into ceil(len_b / C) chunks [c C, min(c C + C, len_b)).  Returns
+    ``(C, [(b, lo, hi), ...])`` in batch order.  This splits the KV sequence of
+    each user as the kernbench2 decode family does (statically sharded KV,
+    partial states reduced per user); the chunk rule is this library's reading
+    (the pages size shards by device count, which has no one-GPU analogue)."""
+    lens = [min(max(int(n), 0), int(max_seqlen)) for n in seqlens]
+    total = sum(lens)
+    c = -(-total * int(hkv) // int(target))
+    c = -(-c // granule) * granule
+    c = max(c, min_chunk)
+    items = []
+    for b, n in enumerate(lens):
+        for lo in range(0, n, c):
+            items.append((b, lo, min(lo + c, n)))
+    return c, items
+
+
 def decode_partials(q, kcache, vcache, seqlens, scale, num_splits):
     """Per-split partial states: ``o_parts [B, Hq, S, d]`` (each normalised by its
     own sum) and ``lse_parts [B, Hq, S]`` (-inf for an empty split)."""

@@ -194,3 +194,27 @@ def test_backward_workspace_size(L):
     assert attn.attn_bwd_workspace_bytes(1, 2, 256) == 2 * 2 * 256 * 4
     assert attn.attn_bwd_workspace_bytes(2, 3, 129) == 2 * 2 * 3 * 256 * 4  # rows padded to 128
     assert attn.attn_bwd_workspace_bytes(0, 2, 256) == 0
+
+
+def _dvl(**kw):
+    a = dict(q=A16, k=A16, v=A16, seqlens=A16, o=A16, B=2, Hq=64, Hkv=8, d=128, scale=0.1, s_max=1024,
+             ws=A16, ws_bytes=1 << 30, stream=0)
+    a.update(kw)
+    return attn.attn_decode_varlen(a["q"], a["k"], a["v"], a["seqlens"], a["o"], a["B"], a["Hq"], a["Hkv"],
+                                   a["d"], a["scale"], a["s_max"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_ARG),
+    (dict(seqlens=A16 + 2), attn.ATTN_ERR_ARG),
+    (dict(B=0), attn.ATTN_ERR_ARG),
+    (dict(Hq=12, Hkv=8), attn.ATTN_ERR_ARG),
+    (dict(s_max=0), attn.ATTN_ERR_ARG),
+    (dict(scale=float("inf")), attn.ATTN_ERR_ARG),
+    (dict(d=56), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Hq=64, Hkv=2), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(ws=None), attn.ATTN_ERR_WORKSPACE),
+    (dict(ws=A16 + 8), attn.ATTN_ERR_WORKSPACE),
+])
+def test_varlen_decode_argument_errors(L, kw, code):
+    assert _dvl(**kw) == code

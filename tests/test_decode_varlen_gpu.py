@@ -1,0 +1,95 @@
+"""GPU parity of the ragged multi-user decode (attn_decode_varlen) through the
+C ABI: outputs against the fp64 oracle, the device work list against the
+oracle's plan (integers, bit-exact), and agreement with attn_decode."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic_inputs import decode_inputs
+from tests.gpu_util import assert_close, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def attn():
+    from attention_fa2_fwd_sm_gb300 import _build
+    _build.build()
+    import attention_fa2_fwd_sm_gb300 as A
+    A.lib()
+    oracle.build()
+    return A
+
+
+def _target():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return max(1, (5 * sms) // 3)
+
+
+CASES = [  # Hq, Hkv, d, s_max, seqlens
+    (64, 8, 128, 20000, [0, 1, 63, 64, 65, 1000, 4096, 20000, 130]),
+    (32, 2, 64, 3000, [3000, 17, 0, 2999, 512, 513]),
+    (8, 8, 128, 5000, [5000, 4, 2500]),
+    (64, 8, 128, 32768, [32768, 100, 2000, 0, 5000, 64, 777, 32767]),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,s_max,lens", CASES)
+def test_ragged_batches_match_the_oracle_and_the_plan(attn, Hq, Hkv, d, s_max, lens):
+    dev = torch.device("cuda")
+    B = len(lens)
+    q, kc, vc = decode_inputs(41, B, Hq, Hkv, s_max, d, dev)
+    seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+    o, ws = attn.decode_varlen(q, kc, vc, seq)
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == attn.ATTN_OK
+    o_ref, _ = oracle.decode(to64(q), to64(kc), to64(vc), lens, d ** -0.5)
+    assert_close(to64(o), o_ref, what=f"varlen {lens}")
+    # the work list the device built, read from the documented workspace head
+    c_ref, items_ref = oracle.varlen_plan(lens, s_max, Hkv, _target())
+    head = ws[: 4 * (2 + 2 * B + 3 * len(items_ref))].view(torch.int32).cpu().tolist()
+    assert head[0] == len(items_ref) and head[1] == c_ref
+    items = [tuple(head[2 + 2 * B + 3 * i: 5 + 2 * B + 3 * i]) for i in range(head[0])]
+    assert items == items_ref
+    first = [sum(1 for b2, _, _ in items_ref if b2 < b) for b in range(B)]
+    assert head[2:2 + B] == first
+    assert head[2 + B:2 + 2 * B] == [sum(1 for b2, _, _ in items_ref if b2 == b) for b in range(B)]
+
+
+def test_agrees_with_the_split_decode(attn):
+    dev = torch.device("cuda")
+    lens = [9000, 10, 4100, 0, 7000]
+    B, Hq, Hkv, d, s_max = len(lens), 64, 8, 128, 9000
+    q, kc, vc = decode_inputs(42, B, Hq, Hkv, s_max, d, dev)
+    seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+    o_v, _ = attn.decode_varlen(q, kc, vc, seq)
+    o_s, _, _ = attn.decode(q, kc, vc, seq)
+    torch.cuda.synchronize()
+    diff = (o_v.float() - o_s.float()).abs().max().item()
+    assert diff <= 2e-2
+    assert torch.count_nonzero(o_v[3]) == 0  # empty sequence -> zeros in both
+    assert torch.count_nonzero(o_s[3]) == 0
+
+
+def test_all_sequences_empty_gives_zeros(attn):
+    dev = torch.device("cuda")
+    q, kc, vc = decode_inputs(43, 4, 16, 4, 256, 64, dev)
+    seq = torch.zeros(4, dtype=torch.int32, device=dev)
+    o, ws = attn.decode_varlen(q, kc, vc, seq)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(o) == 0
+    assert ws[:8].view(torch.int32).tolist() == [0, 512]
+
+
+def test_two_calls_in_a_row_reuse_the_workspace(attn):
+    dev = torch.device("cuda")
+    B, Hq, Hkv, d, s_max = 3, 16, 2, 128, 4000
+    q, kc, vc = decode_inputs(44, B, Hq, Hkv, s_max, d, dev)
+    ws = None
+    for lens in ([4000, 1, 300], [0, 4000, 2222]):
+        seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+        o, ws = attn.decode_varlen(q, kc, vc, seq, workspace=ws)
+        torch.cuda.synchronize()
+        o_ref, _ = oracle.decode(to64(q), to64(kc), to64(vc), lens, d ** -0.5)
+        assert_close(to64(o), o_ref, what=f"{lens}")
