@@ -32,9 +32,11 @@
 // the same time on one Attention Compute Cluster, so the operand they all
 // stream (the group's Q/dO in dkdv, the head's K/V in dq) is read from HBM
 // about once and then served by L2 (detail page, section 2 Q2).
-// Roles (256 threads): warp 0 TMA producer, warp 1 tcgen05 issuer and TMEM
-// owner, warps 2-3 idle, warps 4-7 elementwise / epilogue (warp w owns TMEM
-// lanes [32 (w % 4), +32): one row of the tile per thread).
+// Roles (384 threads): warp 0 TMA producer, warp 1 tcgen05 issuer and TMEM
+// owner, warps 2-3 idle, warps 4-11 elementwise / epilogue.  Warp w owns TMEM
+// lanes [32 (w % 4), +32), one row of the tile per thread; the two warps of a
+// lane quarter split the row's 128 columns (and, in the epilogue, the D
+// output columns) between them.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -57,8 +59,22 @@ static __device__ unsigned int g_bwd_work[kBwdSchedSlots][2][2];
 namespace bwd {
 
 constexpr int kRows = 128;     // rows per tile (keys in dkdv, queries in dq)
-constexpr int kThreads = 256;  // 8 warps
+constexpr int kThreads = 384;  // 12 warps: 4 control, 8 elementwise
+constexpr int kEwWarps = 8;    // two per TMEM lane quarter, each on half of the columns
 constexpr int kTmemCols = 512;
+// Register split after set-up (as in the forward kernel): the launch gives
+// 168 registers per thread; the control warpgroup drops to 104 and the two
+// elementwise warpgroups rise to 200 (128 x 104 + 256 x 200 = 384 x 168).
+// The host refuses a build whose launch register count differs.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 104;
+constexpr int kEwRegs = 200;
+static_assert(128 * kCtrlRegs + 256 * kEwRegs <= kThreads * kLaunchRegs, "register split");
+// dq pass: bf16 dS of the 128-column fp32 S tile is written at column offset
+// 32 of it (64 columns), so a warp only overwrites columns that it has
+// already read: the warp on columns [0, 64) writes [32, 64), the one on
+// [64, 128) writes [64, 96).
+constexpr int kPackOff = 32;
 
 struct Params {
     __nv_bfloat16 *out0, *out1;  // dkdv: dK, dV; dq: dQ (out1 unused)
@@ -177,13 +193,15 @@ __device__ __forceinline__ void finish_schedule(const Params &p, int kernel) {
     }
 }
 
-// Store one row of a TMEM accumulator (D fp32 columns at `t_row`) to global
-// memory as bf16, multiplied by `mul`; columns at or past d_store are clipped.
+// Store half `half` of the columns of one row of a TMEM accumulator (D fp32
+// columns at `t_row`) to global memory as bf16, multiplied by `mul`; columns
+// at or past d_store are clipped.
 template <int D>
-__device__ __forceinline__ void store_row(uint32_t t_row, __nv_bfloat16 *dst, bool row_ok, int d_store,
-                                          float mul) {
+__device__ __forceinline__ void store_half_row(uint32_t t_row, int half, __nv_bfloat16 *dst, bool row_ok,
+                                               int d_store, float mul) {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = half * (D / 64) + cc;  // 32-column chunk
         uint32_t v[32];
         tmem_ld32(t_row + c * 32, v);
         tmem_wait_ld();
@@ -222,16 +240,18 @@ struct KvCfg {
     static constexpr int kTileBytes = kRows * D * 2;   // one 128 x D bf16 tile
     static constexpr int kStages = (D == 128) ? 2 : 3; // Q/dO ring
     static constexpr int kStageBytes = 2 * kTileBytes + 1024;  // Q, dO, lse2, Delta
-    // barriers: kv_full kv_empty st_full[S] st_empty[S] s_full p_full acc_full
-    //           acc_empty uq_full[2] uq_empty[2] drain
+    // barriers: kv_full kv_empty st_full[S] st_empty[S] s_full[2] p_full[2]
+    //           acc_full acc_empty uq_full[2] uq_empty[2] drain
     static constexpr int kBarKVFull = 0, kBarKVEmpty = 1, kBarStFull = 2, kBarStEmpty = 2 + kStages,
-                         kBarSFull = 2 + 2 * kStages, kBarPFull = 3 + 2 * kStages,
-                         kBarAccFull = 4 + 2 * kStages, kBarAccEmpty = 5 + 2 * kStages,
-                         kBarUQFull = 6 + 2 * kStages, kBarUQEmpty = 8 + 2 * kStages,
-                         kBarDrain = 10 + 2 * kStages, kNumBars = 11 + 2 * kStages;
+                         kBarSFull = 2 + 2 * kStages, kBarPFull = 4 + 2 * kStages,
+                         kBarAccFull = 6 + 2 * kStages, kBarAccEmpty = 7 + 2 * kStages,
+                         kBarUQFull = 8 + 2 * kStages, kBarUQEmpty = 10 + 2 * kStages,
+                         kBarDrain = 12 + 2 * kStages, kNumBars = 13 + 2 * kStages;
     static constexpr int kDataBytes = 2 * kTileBytes + kStages * kStageBytes;
     static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 32 + 1024;
-    static constexpr int kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    // TMEM: half-buffer h (query rows [64 h, 64 h + 64) of a block) holds S^T
+    // at [128 h, +64) and dP^T at [128 h + 64, +64); dV and dK follow.
+    static constexpr int kColHalf = 128, kColDV = 256, kColDK = 256 + D;
 };
 
 // Query blocks per query head that key block j meets (causal: i >= j).
@@ -268,15 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(C::kBarKVEmpty), 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(C::kBarStFull + s), 1);
-            mbar_init(bar(C::kBarStEmpty + s), 1 + 4);  // MMA commit + 4 elementwise warps
+            mbar_init(bar(C::kBarStEmpty + s), 1 + kEwWarps);  // MMA commit + elementwise warps
         }
-        mbar_init(bar(C::kBarSFull), 1);
-        mbar_init(bar(C::kBarPFull), 4);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(C::kBarSFull + h), 1);
+            mbar_init(bar(C::kBarPFull + h), kEwWarps / 2);  // the half's warpgroup
+        }
         mbar_init(bar(C::kBarAccFull), 1);
-        mbar_init(bar(C::kBarAccEmpty), 4);
+        mbar_init(bar(C::kBarAccEmpty), kEwWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(C::kBarUQFull + i), 1);
-            mbar_init(bar(C::kBarUQEmpty + i), 1 + 4);  // MMA thread + 4 elementwise warps
+            mbar_init(bar(C::kBarUQEmpty + i), 1 + kEwWarps);  // MMA thread + elementwise warps
         }
         mbar_init(bar(C::kBarDrain), 1);
         *abort_flag = 0;
@@ -298,7 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     int *status = &g_bwd_status;
 
-    if (warp == 0) {
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+      if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             long long fills = 0;  // ring fills issued
@@ -377,14 +401,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
+        // Per 128-row query block (one ring stage) and half h (its query rows
+        // [64 h, 64 h + 64)): S^T_h = K Q_h^T and dP^T_h = V dO_h^T into
+        // half-buffer h, then, once warpgroup h has written P^T_h and dS^T_h,
+        // dV += P^T_h dO_h and dK += dS^T_h Q_h.  Issue order per stage t:
+        //   dVdK(0, t), S(0, t+1), dVdK(1, t), S(1, t+1)
+        // so the tensor core works on one half while warpgroup h computes the
+        // other, and the commit announcing S(h, t+1) also covers dVdK(h, t).
         if (lane == 0) {
-            constexpr uint32_t kIdescS = idesc_bf16_f32(kRows, kRows, 0);  // K-major A and B
-            constexpr uint32_t kIdescAcc = idesc_bf16_f32(kRows, D, 1);    // B read MN-major
+            constexpr uint32_t kIdescS = idesc_bf16_f32(kRows, 64, 0);  // N = 64 query rows
+            constexpr uint32_t kIdescAcc = idesc_bf16_f32(kRows, D, 1);  // B read MN-major
             const uint64_t dK0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t dV0 = smem_desc_sw128(smem_u32(sV), 16, 1024);
             long long fills = 0;
-            int kv_used = 0, p_waits = 0, units_done = 0;
+            int kv_used = 0, units_done = 0;
+            int p_waits[2] = {0, 0};
             bool ok = true;
+            auto wait_stage = [&](long long f) {
+                return mbar_wait_bounded(bar(C::kBarStFull + int(f % C::kStages)), uint32_t((f / C::kStages) & 1),
+                                         p.wait_ns, abort_flag, status);
+            };
+            // S^T_h and dP^T_h of the stage at ring position f.
+            auto issue_s = [&](int h, long long f) {
+                const int slot = int(f % C::kStages);
+                const uint32_t hrow = uint32_t(h * 64 * 128);  // byte offset of row 64 h in a chunk
+                const uint64_t dQk = smem_desc_sw128(smem_u32(stage_q(slot)) + hrow, 16, 1024);
+                const uint64_t dOk = smem_desc_sw128(smem_u32(stage_do(slot)) + hrow, 16, 1024);
+                const uint32_t tS = tmem_base + h * C::kColHalf;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
+                    tc_mma_ss(tS, dK0 + off, dQk + off, kIdescS, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
+                    tc_mma_ss(tS + 64, dV0 + off, dOk + off, kIdescS, kk > 0);
+                }
+                tc_commit(bar(C::kBarSFull + h));
+            };
             for (long long qi = 0; ok; ++qi) {
                 const int qs = int(qi & 1);
                 ok = mbar_wait_bounded(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag,
@@ -396,52 +451,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const KvUnit w = kv_unit(p, u);
                 const int iters = p.G * (p.nblk - kv_first_i(p, w.j));
                 ok = mbar_wait_bounded(bar(C::kBarKVFull), uint32_t(kv_used & 1), p.wait_ns, abort_flag, status);
+                if (ok) ok = wait_stage(fills);
                 if (!ok) break;
                 ++kv_used;
+                tc_fence_after();
+                issue_s(0, fills);
+                issue_s(1, fills);
                 for (int t = 0; ok && t < iters; ++t) {
                     const int slot = int(fills % C::kStages);
-                    ok = mbar_wait_bounded(bar(C::kBarStFull + slot), uint32_t((fills / C::kStages) & 1),
-                                           p.wait_ns, abort_flag, status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t dQk = smem_desc_sw128(smem_u32(stage_q(slot)), 16, 1024);
-                    const uint64_t dOk = smem_desc_sw128(smem_u32(stage_do(slot)), 16, 1024);
-                    // S^T = K Q^T and dP^T = V dO^T (K steps over the head dimension)
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-                        tc_mma_ss(tmem_base + C::kColS, dK0 + off, dQk + off, kIdescS, kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-                        tc_mma_ss(tmem_base + C::kColDP, dV0 + off, dOk + off, kIdescS, kk > 0);
-                    }
-                    tc_commit(bar(C::kBarSFull));
-                    ok = mbar_wait_bounded(bar(C::kBarPFull), uint32_t(p_waits & 1), p.wait_ns, abort_flag, status);
-                    if (!ok) break;
-                    ++p_waits;
-                    if (t == 0 && units_done > 0) {
-                        ok = mbar_wait_bounded(bar(C::kBarAccEmpty), uint32_t((units_done - 1) & 1), p.wait_ns,
+                    const bool has_next = t + 1 < iters;
+                    for (int h = 0; h < 2; ++h) {
+                        ok = mbar_wait_bounded(bar(C::kBarPFull + h), uint32_t(p_waits[h] & 1), p.wait_ns,
                                                abort_flag, status);
                         if (!ok) break;
+                        ++p_waits[h];
+                        if (t == 0 && h == 0 && units_done > 0) {
+                            ok = mbar_wait_bounded(bar(C::kBarAccEmpty), uint32_t((units_done - 1) & 1), p.wait_ns,
+                                                   abort_flag, status);
+                            if (!ok) break;
+                        }
+                        tc_fence_after();
+                        const uint32_t hrow = uint32_t(h * 64 * 128);
+                        const uint64_t dOmn = smem_desc_sw128(smem_u32(stage_do(slot)) + hrow, C::kChunkBytes, 1024);
+                        const uint64_t dQmn = smem_desc_sw128(smem_u32(stage_q(slot)) + hrow, C::kChunkBytes, 1024);
+                        const uint32_t tH = tmem_base + h * C::kColHalf;
+                        const bool first = (t == 0 && h == 0);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)  // K = 64 query rows
+                            tc_mma_ts(tmem_base + C::kColDV, tH + kk * 8, dOmn + uint64_t((kk * 16 * 128) >> 4),
+                                      kIdescAcc, (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma_ts(tmem_base + C::kColDK, tH + 64 + kk * 8, dQmn + uint64_t((kk * 16 * 128) >> 4),
+                                      kIdescAcc, (!first || kk > 0) ? 1u : 0u);
+                        if (h == 1) tc_commit(bar(C::kBarStEmpty + slot));
+                        if (has_next) {
+                            if (h == 0) {
+                                ok = wait_stage(fills + 1);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            issue_s(h, fills + 1);
+                        }
                     }
-                    tc_fence_after();
-                    // dV += P^T dO and dK += dS^T Q (K steps over the 128 query rows;
-                    // P^T / dS^T bf16 in TMEM, dO / Q read MN-major)
-                    const uint64_t dOmn = smem_desc_sw128(smem_u32(stage_do(slot)), C::kChunkBytes, 1024);
-                    const uint64_t dQmn = smem_desc_sw128(smem_u32(stage_q(slot)), C::kChunkBytes, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < kRows / 16; ++kk)
-                        tc_mma_ts(tmem_base + C::kColDV, tmem_base + C::kColS + kk * 8,
-                                  dOmn + uint64_t((kk * 16 * 128) >> 4), kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < kRows / 16; ++kk)
-                        tc_mma_ts(tmem_base + C::kColDK, tmem_base + C::kColDP + kk * 8,
-                                  dQmn + uint64_t((kk * 16 * 128) >> 4), kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar(C::kBarStEmpty + slot));
+                    if (!ok) break;
                     ++fills;
-                    if (t == iters - 1) {
+                    if (!has_next) {
                         tc_commit(bar(C::kBarAccFull));
                         tc_commit(bar(C::kBarKVEmpty));
                         ++units_done;
@@ -454,13 +509,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(status, kStatusDrainTimeout);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEwRegs));
         // ---------------------------------------------------------------- elementwise / epilogue
+        // Warpgroup h = (w - 4) / 4 owns half-buffer h: query rows [64 h, +64)
+        // of every block; warp w reads TMEM lanes [32 (w % 4), +32), one key
+        // row per thread.
         const int quarter = warp & 3;
+        const int half = (warp - 4) >> 2;
         const int r = quarter * 32 + lane;  // key row inside the block
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-        const uint32_t tS = tmem_base + lane_off + C::kColS;
-        const uint32_t tDP = tmem_base + lane_off + C::kColDP;
+        const uint32_t tH = tmem_base + lane_off + half * C::kColHalf;  // S^T_h; dP^T_h at +64
         const float sl2 = p.scale_log2;
         long long fills = 0;
         int s_waits = 0, acc_waits = 0;
@@ -480,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < iters; ++t) {
                 const int i = i0 + t % ni;
                 const int slot = int(fills % C::kStages);
-                ok = mbar_wait_warp(bar(C::kBarSFull), uint32_t(s_waits & 1), p.wait_ns, abort_flag, status);
+                ok = mbar_wait_warp(bar(C::kBarSFull + half), uint32_t(s_waits & 1), p.wait_ns, abort_flag, status);
                 // The stage's lse / Delta rows: wait on the stage's own fill barrier
                 // (already complete, since the MMA thread waited on it first).
                 if (ok)
@@ -489,15 +549,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 ++s_waits;
                 tc_fence_after();
-                const float4 *l4 = reinterpret_cast<const float4 *>(stage_l(slot));
-                const float4 *d4 = reinterpret_cast<const float4 *>(stage_l(slot) + kRows);
-                const bool diag = p.causal && i == w.j;  // query rows before this key are masked
+                uint32_t sv[2][32], dv[2][32];
 #pragma unroll
-                for (int c = 0; c < kRows / 32; ++c) {
-                    uint32_t sv[32], dv[32];
-                    tmem_ld32(tS + c * 32, sv);
-                    tmem_ld32(tDP + c * 32, dv);
-                    tmem_wait_ld();
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(tH + c * 32, sv[c]);
+                    tmem_ld32(tH + 64 + c * 32, dv[c]);
+                }
+                const float4 *l4 = reinterpret_cast<const float4 *>(stage_l(slot)) + half * 16;
+                const float4 *d4 = reinterpret_cast<const float4 *>(stage_l(slot) + kRows) + half * 16;
+                const bool diag = p.causal && i == w.j;  // query rows before this key are masked
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int q0 = half * 64 + c * 32;  // first query row of the chunk
                     uint32_t pk[16], dk[16];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -509,35 +573,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int k = 0; k < 4; k += 2) {
                             float x0, x1;
-                            ffma2(x0, x1, __uint_as_float(sv[4 * e + k]), __uint_as_float(sv[4 * e + k + 1]), sl2,
-                                  sl2, -lv[k], -lv[k + 1]);
+                            ffma2(x0, x1, __uint_as_float(sv[c][4 * e + k]), __uint_as_float(sv[c][4 * e + k + 1]),
+                                  sl2, sl2, -lv[k], -lv[k + 1]);
                             pr[k] = fast_exp2(x0);
                             pr[k + 1] = fast_exp2(x1);
                         }
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            if (diag && c * 32 + 4 * e + k < r) pr[k] = 0.f;
-                            ds[k] = pr[k] * (__uint_as_float(dv[4 * e + k]) - dl[k]);
+                            if (diag && q0 + 4 * e + k < r) pr[k] = 0.f;
+                            ds[k] = pr[k] * (__uint_as_float(dv[c][4 * e + k]) - dl[k]);
                         }
                         pk[2 * e] = pack_bf16x2(pr[0], pr[1]);
                         pk[2 * e + 1] = pack_bf16x2(pr[2], pr[3]);
                         dk[2 * e] = pack_bf16x2(ds[0], ds[1]);
                         dk[2 * e + 1] = pack_bf16x2(ds[2], ds[3]);
                     }
-                    tmem_st16(tS + c * 16, pk);
-                    tmem_st16(tDP + c * 16, dk);
+                    // bf16 pairs over the half's own fp32 columns, all read above
+                    tmem_st16(tH + c * 16, pk);
+                    tmem_st16(tH + 64 + c * 16, dk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar(C::kBarPFull));
+                    mbar_arrive(bar(C::kBarPFull + half));
                     mbar_arrive(bar(C::kBarStEmpty + slot));
                 }
                 ++fills;
             }
             if (!ok) break;
-            // Epilogue: dV and scale * dK of this thread's key row -> bf16.
+            // Epilogue: dV and scale * dK of this thread's key row -> bf16; the
+            // two warpgroups store one half of the columns each.
             ok = mbar_wait_warp(bar(C::kBarAccFull), uint32_t(acc_waits & 1), p.wait_ns, abort_flag, status);
             if (!ok) break;
             ++acc_waits;
@@ -545,8 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key = w.j * kRows + r;
             const bool row_ok = key < p.N;
             const size_t off = ((size_t)(w.b * p.Hkv + w.g) * p.N + (row_ok ? key : 0)) * p.d_store;
-            store_row<D>(tmem_base + lane_off + C::kColDV, p.out1 + off, row_ok, p.d_store, 1.f);
-            store_row<D>(tmem_base + lane_off + C::kColDK, p.out0 + off, row_ok, p.d_store, p.scale);
+            store_half_row<D>(tmem_base + lane_off + C::kColDV, half, p.out1 + off, row_ok, p.d_store, 1.f);
+            store_half_row<D>(tmem_base + lane_off + C::kColDK, half, p.out0 + off, row_ok, p.d_store, p.scale);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarAccEmpty));
@@ -617,12 +683,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::kBarKVEmpty + s), 1);
         }
         mbar_init(bar(C::kBarSFull), 1);
-        mbar_init(bar(C::kBarPFull), 4);
+        mbar_init(bar(C::kBarPFull), kEwWarps);
         mbar_init(bar(C::kBarAccFull), 1);
-        mbar_init(bar(C::kBarAccEmpty), 4);
+        mbar_init(bar(C::kBarAccEmpty), kEwWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(C::kBarUQFull + i), 1);
-            mbar_init(bar(C::kBarUQEmpty + i), 1 + 4);
+            mbar_init(bar(C::kBarUQEmpty + i), 1 + kEwWarps);
         }
         mbar_init(bar(C::kBarDrain), 1);
         *abort_flag = 0;
@@ -644,7 +710,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     int *status = &g_bwd_status;
 
-    if (warp == 0) {
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+      if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             long long fills = 0;
@@ -765,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t dKmn = smem_desc_sw128(smem_u32(stage_k(slot)), C::kChunkBytes, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kRows / 16; ++kk)
-                        tc_mma_ts(tmem_base + C::kColDQ, tmem_base + C::kColS + kk * 8,
+                        tc_mma_ts(tmem_base + C::kColDQ, tmem_base + C::kColS + kPackOff + kk * 8,
                                   dKmn + uint64_t((kk * 16 * 128) >> 4), kIdescAcc, (j > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar(C::kBarKVEmpty + slot));
                     ++fills;
@@ -782,9 +850,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(status, kStatusDrainTimeout);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEwRegs));
         // ---------------------------------------------------------------- elementwise / epilogue
+        // Two warps per TMEM lane quarter: warp w reads query rows
+        // [32 (w % 4), +32) and the key columns [64 h, 64 h + 64),
+        // h = (w - 4) / 4.  dS (bf16) goes to columns [32, 96) of S, so each
+        // warp overwrites only columns that it has already read.
         const int quarter = warp & 3;
+        const int half = (warp - 4) >> 2;
         const int r = quarter * 32 + lane;  // query row inside the block
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
         const uint32_t tS = tmem_base + lane_off + C::kColS;
@@ -811,31 +886,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 ++s_waits;
                 tc_fence_after();
-                const int kv0 = j * kRows;
-                const bool ragged = kv0 + kRows > p.N;
-                const bool diag = p.causal && j == w.i;
-                int lim = kRows;  // keys kv0 + c with c >= lim are masked
-                if (ragged) lim = p.N - kv0;
-                if (diag) lim = min(lim, r + 1);
+                // Both chunks of this warp's half are read before anything is
+                // written (the first chunk's bf16 lands on the second's columns).
+                uint32_t sv[2][32], dv[2][32];
 #pragma unroll
-                for (int c = 0; c < kRows / 32; ++c) {
-                    uint32_t sv[32], dv[32];
-                    tmem_ld32(tS + c * 32, sv);
-                    tmem_ld32(tDP + c * 32, dv);
-                    tmem_wait_ld();
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(tS + (2 * half + c) * 32, sv[c]);
+                    tmem_ld32(tDP + (2 * half + c) * 32, dv[c]);
+                }
+                const int kv0 = j * kRows;
+                int lim = kRows;  // block columns c >= lim are masked (past N or after the row)
+                if (kv0 + kRows > p.N) lim = p.N - kv0;
+                if (p.causal && j == w.i) lim = min(lim, r + 1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int k0 = (2 * half + c) * 32;  // first block column of the chunk
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         float x0, x1;
-                        ffma2(x0, x1, __uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]), sl2, sl2, neg_l,
-                              neg_l);
+                        ffma2(x0, x1, __uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1]), sl2, sl2,
+                              neg_l, neg_l);
                         float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                        if (c * 32 + 2 * e >= lim) p0 = 0.f;
-                        if (c * 32 + 2 * e + 1 >= lim) p1 = 0.f;
-                        pk[e] = pack_bf16x2(p0 * (__uint_as_float(dv[2 * e]) - del),
-                                            p1 * (__uint_as_float(dv[2 * e + 1]) - del));
+                        if (k0 + 2 * e >= lim) p0 = 0.f;
+                        if (k0 + 2 * e + 1 >= lim) p1 = 0.f;
+                        pk[e] = pack_bf16x2(p0 * (__uint_as_float(dv[c][2 * e]) - del),
+                                            p1 * (__uint_as_float(dv[c][2 * e + 1]) - del));
                     }
-                    tmem_st16(tS + c * 16, pk);
+                    tmem_st16(tS + kPackOff + k0 / 2, pk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -849,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool row_ok = row < p.N;
             const size_t off = ((size_t)(w.b * p.Hq + w.h) * p.N + (row_ok ? row : 0)) * p.d_store;
-            store_row<D>(tmem_base + lane_off + C::kColDQ, p.out0 + off, row_ok, p.d_store, p.scale);
+            store_half_row<D>(tmem_base + lane_off + C::kColDQ, half, p.out0 + off, row_ok, p.d_store, p.scale);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarAccEmpty));
@@ -897,8 +976,17 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
 
     static bool attr_set = false;  // per instantiation
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             CA::kSmemBytes);
+        // The setmaxnreg split assumes the launch register count; refuse a
+        // build that differs (its setmaxnreg.inc could never complete).
+        cudaFuncAttributes fa, fb;
+        cudaError_t e = cudaFuncGetAttributes(&fa, dkdv_kernel<D>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fb, dq_kernel<D>);
+        if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncGetAttributes(backward kernels)");
+        if (fa.numRegs != kLaunchRegs || fb.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads ||
+            fb.maxThreadsPerBlock < kThreads)
+            return note_cuda_error(cudaErrorInvalidConfiguration,
+                                   "backward kernel register count differs from the setmaxnreg split");
+        e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CA::kSmemBytes);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CB::kSmemBytes);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(backward kernels)");
