@@ -648,6 +648,49 @@ def run_decode_varlen(args):
         torch.cuda.empty_cache()
 
 
+def run_bwd_sweep(args):
+    """Backward configurations (MHA, GQA causal and non-causal, DeepSeek-like
+    d=56 causal) in the head-first and block-first orders; one JSON line per
+    configuration."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import output_grad, prefill_inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    configs = []
+    for N in (8192, 32768):
+        configs.append(("mha", 1, 128, 128, N, 128, False))
+        for causal in (False, True):
+            configs.append(("gqa", 1, 64, 8, N, 128, causal))
+    configs.append(("deepseek", 1, 128, 128, 32768, 56, True))
+    for name, B, Hq, Hkv, N, d, causal in configs:
+        q, k, v = prefill_inputs(15, B, Hq, Hkv, N, d, dev)
+        dout = output_grad(15, B, Hq, N, d, dev)
+        o, lse = attn.forward(q, k, v, causal=causal, scale=d ** -0.5)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        nbytes = attn.attn_bwd_workspace_bytes(B, Hq, N)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        flops = bwd_flops(B, Hq, N, d, causal)
+        out = {"mode": "bwd-sweep", "config": name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
+               "causal": causal, "flops": flops}
+        for oname in ("head_first", "block_first"):
+            oid = attn.ORDERS[oname]
+            fn = lambda: attn.check(attn.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, d ** -0.5,
+                                                  causal, oid, ws, nbytes, stream.cuda_stream), "bwd")
+            fn()
+            ms = _time_calls(torch, fn, args.steps, None, stream)
+            tf = flops / (ms / 1e3) / 1e12
+            out[oname] = {"ms": round(ms, 3), "tflops": round(tf, 1), "frac": round(tf / peaks["bf16_tflops"], 4)}
+        print(json.dumps(out), flush=True)
+        del q, k, v, dout, o, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+
+
 def run_die_map(args):
     """The SM -> die map the die-split order uses (measured on first use) with
     its calibration statistics; one JSON line."""
@@ -672,7 +715,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--mode", default="step",
                     choices=["step", "decode-sweep", "decode-varlen", "fwd-sweep", "fwd-one", "bwd-one",
-                             "die-map"],
+                             "bwd-sweep", "die-map"],
                     help="step: the contract's one-line benchmark; the sweeps print one line "
                          "per configuration; fwd-one times one forward configuration")
     ap.add_argument("--batch", type=int, default=1, help="fwd-one: batch")
@@ -705,6 +748,8 @@ def main():
         return run_bwd_one(args)
     if args.mode == "decode-varlen":
         return run_decode_varlen(args)
+    if args.mode == "bwd-sweep":
+        return run_bwd_sweep(args)
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)
