@@ -321,14 +321,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto slot_off = [&](long long f) {
                 return uint64_t(int(f % C::kStages) * (C::kKVBytes >> 4));
             };
+            // Each group of MMAs goes out from one asm block (descriptors
+            // computed first), so the issuing thread needs no issue slots
+            // between them while the softmax warps of its sub-partition run.
             auto issue_qk = [&](int t, long long fK) {
                 const uint64_t a0 = dQ + uint64_t(t * (C::kQBytes >> 4));
                 const uint64_t b0 = dK + slot_off(fK);
                 const uint32_t d_tmem = tmem_base + t * kTileM;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-                    tc_mma_ss(d_tmem, a0 + off, b0 + off, kIdescQK, kk > 0);
+                for (int g = 0; g < D / 64; ++g) {  // four K=16 steps per 128-byte chunk
+                    uint64_t a[4], b[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint64_t off = uint64_t((g * C::kChunkBytes + i * 32) >> 4);
+                        a[i] = a0 + off;
+                        b[i] = b0 + off;
+                    }
+                    tc_mma_ss_x4(d_tmem, a, b, kIdescQK, g > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, long long fV, bool acc) {
@@ -336,9 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d_tmem = tmem_base + C::kOCol + t * D;
                 const uint32_t a_tmem = tmem_base + t * kTileM;
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    tc_mma_ts(d_tmem, a_tmem + kk * 8, b0 + uint64_t((kk * 16 * 128) >> 4), kIdescPV,
-                              (acc || kk > 0) ? 1u : 0u);
+                for (int g = 0; g < kBlockN / 64; ++g) {
+                    uint32_t a[4];
+                    uint64_t b[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int kk = g * 4 + i;
+                        a[i] = a_tmem + kk * 8;
+                        b[i] = b0 + uint64_t((kk * 16 * 128) >> 4);
+                    }
+                    tc_mma_ts_x4(d_tmem, a, b, kIdescPV, (acc || g > 0) ? 1u : 0u);
                 }
             };
 
