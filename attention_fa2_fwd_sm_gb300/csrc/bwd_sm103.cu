@@ -221,6 +221,41 @@ __device__ __forceinline__ void store_half_row(uint32_t t_row, int half, __nv_bf
     }
 }
 
+// D (+)= A B^T over the head dimension (K-major A and B in 128-byte-swizzled
+// 64-column chunks), issued in groups of four MMAs from one asm block.
+template <int D, int kChunkBytes>
+__device__ __forceinline__ void ss_product(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
+#pragma unroll
+    for (int g = 0; g < D / 64; ++g) {
+        uint64_t a[4], b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint64_t off = uint64_t((g * kChunkBytes + i * 32) >> 4);
+            a[i] = a0 + off;
+            b[i] = b0 + off;
+        }
+        tc_mma_ss_x4(d_tmem, a, b, idesc, g > 0 ? 1u : 0u);
+    }
+}
+
+// D (+)= A B with A (bf16) in TMEM from column a_tmem and B read MN-major,
+// K = 16 NK rows; the first MMA accumulates iff `acc`.
+template <int NK>
+__device__ __forceinline__ void ts_product(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int g = 0; g < NK / 4; ++g) {
+        uint32_t a[4];
+        uint64_t b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int kk = g * 4 + i;
+            a[i] = a_tmem + kk * 8;
+            b[i] = b0 + uint64_t((kk * 16 * 128) >> 4);
+        }
+        tc_mma_ts_x4(d_tmem, a, b, idesc, (acc || g > 0) ? 1u : 0u);
+    }
+}
+
 // A 1-D bulk copy global -> shared memory completing on an mbarrier (both
 // addresses 16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
@@ -428,16 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dQk = smem_desc_sw128(smem_u32(stage_q(slot)) + hrow, 16, 1024);
                 const uint64_t dOk = smem_desc_sw128(smem_u32(stage_do(slot)) + hrow, 16, 1024);
                 const uint32_t tS = tmem_base + h * C::kColHalf;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-                    tc_mma_ss(tS, dK0 + off, dQk + off, kIdescS, kk > 0);
-                }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-                    tc_mma_ss(tS + 64, dV0 + off, dOk + off, kIdescS, kk > 0);
-                }
+                ss_product<D, C::kChunkBytes>(tS, dK0, dQk, kIdescS);
+                ss_product<D, C::kChunkBytes>(tS + 64, dV0, dOk, kIdescS);
                 tc_commit(bar(C::kBarSFull + h));
             };
             for (long long qi = 0; ok; ++qi) {
@@ -476,14 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t dQmn = smem_desc_sw128(smem_u32(stage_q(slot)) + hrow, C::kChunkBytes, 1024);
                         const uint32_t tH = tmem_base + h * C::kColHalf;
                         const bool first = (t == 0 && h == 0);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)  // K = 64 query rows
-                            tc_mma_ts(tmem_base + C::kColDV, tH + kk * 8, dOmn + uint64_t((kk * 16 * 128) >> 4),
-                                      kIdescAcc, (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc_mma_ts(tmem_base + C::kColDK, tH + 64 + kk * 8, dQmn + uint64_t((kk * 16 * 128) >> 4),
-                                      kIdescAcc, (!first || kk > 0) ? 1u : 0u);
+                        ts_product<4>(tmem_base + C::kColDV, tH, dOmn, kIdescAcc, !first);  // K = 64 query rows
+                        ts_product<4>(tmem_base + C::kColDK, tH + 64, dQmn, kIdescAcc, !first);
                         if (h == 1) tc_commit(bar(C::kBarStEmpty + slot));
                         if (has_next) {
                             if (h == 0) {
@@ -809,16 +830,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t dKk = smem_desc_sw128(smem_u32(stage_k(slot)), 16, 1024);
                     const uint64_t dVk = smem_desc_sw128(smem_u32(stage_v(slot)), 16, 1024);
                     // S = Q K^T and dP = dO V^T
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-                        tc_mma_ss(tmem_base + C::kColS, dQ0 + off, dKk + off, kIdescS, kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = uint64_t(((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4);
-                        tc_mma_ss(tmem_base + C::kColDP, dO0 + off, dVk + off, kIdescS, kk > 0);
-                    }
+                    ss_product<D, C::kChunkBytes>(tmem_base + C::kColS, dQ0, dKk, kIdescS);
+                    ss_product<D, C::kChunkBytes>(tmem_base + C::kColDP, dO0, dVk, kIdescS);
                     tc_commit(bar(C::kBarSFull));
                     ok = mbar_wait_bounded(bar(C::kBarPFull), uint32_t(p_waits & 1), p.wait_ns, abort_flag, status);
                     if (!ok) break;
@@ -831,10 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     // dQ += dS K (dS bf16 in TMEM over S; K read MN-major)
                     const uint64_t dKmn = smem_desc_sw128(smem_u32(stage_k(slot)), C::kChunkBytes, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < kRows / 16; ++kk)
-                        tc_mma_ts(tmem_base + C::kColDQ, tmem_base + C::kColS + kPackOff + kk * 8,
-                                  dKmn + uint64_t((kk * 16 * 128) >> 4), kIdescAcc, (j > 0 || kk > 0) ? 1u : 0u);
+                    ts_product<8>(tmem_base + C::kColDQ, tmem_base + C::kColS + kPackOff, dKmn, kIdescAcc, j > 0);
                     tc_commit(bar(C::kBarKVEmpty + slot));
                     ++fills;
                     if (j == nkv - 1) {

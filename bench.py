@@ -40,11 +40,10 @@ DEC = dict(B=8, Hq=64, Hkv=8, S=32768, d=128)
 # digest; after any change to them the bench reports null until re-captured.
 MEASURED_TRAFFIC = {
     "fwd": {"files": ["fwd_sm103.cu", "sm103_ptx.cuh", "tile_order.cuh"],
-            "sha256": "cc81b7db000337d23377cd1bc98d8d454b3782c1d4ab0f35288827d48cad8523",
+            "sha256": "f85c8ae35f9709b87d0834934a0cb91a11d696fef83048d36c9ced6cded9c49b",
             # MHA B=1 H=128 d=128, head-first, captured at N=32768 and N=8192 (one-pass
-            # capture of dram__bytes_read.sum / dram__bytes_write.sum; the full-size
-            # figures are printed to three significant digits)
-            "bytes_by_n": {32768: 4_320_000_000, 8192: 1_058_070_000}},
+            # capture of dram__bytes_read.sum + dram__bytes_write.sum)
+            "bytes_by_n": {32768: 3233039104 + 1088919296, 8192: 805848576 + 251660032}},
     "decode": {"files": ["decode_sm103.cu", "sm103_ptx.cuh"],
                "sha256": "41e8476af5f5dbf468fb89d766525d8bc21502a58da309f748346aaa6c9f9e33",
                # GQA decode B=8 Hq=64 Hkv=8 d=128, 4 splits, captured at 8192 keys;
