@@ -93,3 +93,23 @@ def test_two_calls_in_a_row_reuse_the_workspace(attn):
         torch.cuda.synchronize()
         o_ref, _ = oracle.decode(to64(q), to64(kc), to64(vc), lens, d ** -0.5)
         assert_close(to64(o), o_ref, what=f"{lens}")
+
+
+def test_many_users_per_plan_thread(attn):
+    """600 users: the plan kernel's threads each take several sequences."""
+    dev = torch.device("cuda")
+    g = torch.Generator().manual_seed(45)
+    lens = torch.randint(0, 700, (600,), generator=g).tolist()
+    lens[7] = 0
+    lens[599] = 700
+    B, Hq, Hkv, d, s_max = len(lens), 8, 2, 64, 700
+    q, kc, vc = decode_inputs(46, B, Hq, Hkv, s_max, d, dev)
+    seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+    o, ws = attn.decode_varlen(q, kc, vc, seq)
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == attn.ATTN_OK
+    c_ref, items_ref = oracle.varlen_plan(lens, s_max, Hkv, _target())
+    head = ws[:8].view(torch.int32).tolist()
+    assert head == [len(items_ref), c_ref]
+    o_ref, _ = oracle.decode(to64(q), to64(kc), to64(vc), lens, d ** -0.5)
+    assert_close(to64(o), o_ref, what="600 users")
