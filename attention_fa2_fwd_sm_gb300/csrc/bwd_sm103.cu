@@ -20,9 +20,12 @@
 //                    S^T = K Q^T and dP^T = V dO^T (SS MMAs into TMEM), P^T
 //                    and dS^T in bf16 written back over them, then dV += P^T dO
 //                    and dK += dS^T Q (TS MMAs, dO and Q read MN-major).
-//   dq_kernel<D>     one unit = 128 query rows of one query head; Q and dO stay
-//                    in shared memory while K/V blocks stream: S = Q K^T and
-//                    dP = dO V^T, dS in bf16 over S, dQ += dS K (TS MMA).
+//   dq_kernel<D>     one unit = 256 query rows of one query head (two 128-row
+//                    tiles sharing every K/V block); Q and dO stay in shared
+//                    memory while K/V blocks stream: S = Q K^T, then dP =
+//                    dO V^T in the same TMEM buffer, dS in bf16 over it,
+//                    dQ += dS K (TS MMA); the two tiles alternate on the
+//                    tensor core.
 // Splitting dQ into its own pass recomputes S and dP (seven products instead of
 // five) but needs no atomic accumulation: every output element is written
 // once, by one CTA, and the result does not depend on the schedule.
@@ -63,12 +66,13 @@ constexpr int kThreads = 384;  // 12 warps: 4 control, 8 elementwise
 constexpr int kEwWarps = 8;    // two per TMEM lane quarter, each on half of the columns
 constexpr int kTmemCols = 512;
 // Register split after set-up (as in the forward kernel): the launch gives
-// 168 registers per thread; the control warpgroup drops to 104 and the two
-// elementwise warpgroups rise to 200 (128 x 104 + 256 x 200 = 384 x 168).
-// The host refuses a build whose launch register count differs.
+// 168 registers per thread; the control warpgroup drops to 128 (the issuers'
+// state) and the two elementwise warpgroups rise to 184
+// (128 x 128 + 256 x 184 <= 384 x 168).  The host refuses a build whose
+// launch register count differs.
 constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 104;
-constexpr int kEwRegs = 200;
+constexpr int kCtrlRegs = 128;
+constexpr int kEwRegs = 184;
 static_assert(128 * kCtrlRegs + 256 * kEwRegs <= kThreads * kLaunchRegs, "register split");
 // dq pass: bf16 dS of the 128-column fp32 S tile is written at column offset
 // 32 of it (64 columns), so a warp only overwrites columns that it has
@@ -650,28 +654,72 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------- dQ
+//
+// One unit is 256 query rows of one query head: two 128-row tiles that share
+// every K/V block (as in the forward kernel) and alternate on the tensor core.
+// TMEM per tile t: one 128-column fp32 buffer X(t) at 128 t that holds S,
+// then dP (dS in bf16 is written over its first 64 columns), and the dQ(t)
+// accumulator at 256 + D t.  Per K/V block j and tile t:
+//   S(t, j) = Q_t K_j^T -> X(t);  warpgroup t keeps P = exp(S - lse) (fp32)
+//   in registers; dP(t, j) = dO_t V_j^T -> X(t); warpgroup t writes
+//   dS = P (dP - Delta) as bf16; dQ(t) += dS K_j.
+// Issue order per block: dP(0, j), dP(1, j), dQ(0, j), S(0, j + 1), dQ(1, j),
+// S(1, j + 1), so one tile's elementwise phase overlaps the other tile's MMAs.
 
 template <int D>
 struct QCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kChunkBytes = kRows * 128;
     static constexpr int kTileBytes = kRows * D * 2;
-    static constexpr int kStages = (D == 128) ? 2 : 4;  // K/V ring (one stage = K_j and V_j)
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    // barriers: q_full q_empty kv_full[S] kv_empty[S] s_full p_full acc_full
-    //           acc_empty uq_full[2] uq_empty[2] drain
-    static constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKVFull = 2, kBarKVEmpty = 2 + kStages,
-                         kBarSFull = 2 + 2 * kStages, kBarPFull = 3 + 2 * kStages,
-                         kBarAccFull = 4 + 2 * kStages, kBarAccEmpty = 5 + 2 * kStages,
-                         kBarUQFull = 6 + 2 * kStages, kBarUQEmpty = 8 + 2 * kStages,
-                         kBarDrain = 10 + 2 * kStages, kNumBars = 11 + 2 * kStages;
-    static constexpr int kDataBytes = 2 * kTileBytes + kStages * kStageBytes;
+    static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring of single tiles (K_j, V_j, K_j+1, ...)
+    // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2]
+    //           dp_full[2] ds_full[2] acc_full[2] acc_empty[2] uq_full[2] uq_empty[2] drain
+    static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKVFull = 4, kBarKVEmpty = 4 + kStages,
+                         kBarSFull = 4 + 2 * kStages, kBarPFull = 6 + 2 * kStages, kBarDPFull = 8 + 2 * kStages,
+                         kBarDSFull = 10 + 2 * kStages, kBarAccFull = 12 + 2 * kStages,
+                         kBarAccEmpty = 14 + 2 * kStages, kBarUQFull = 16 + 2 * kStages,
+                         kBarUQEmpty = 18 + 2 * kStages, kBarDrain = 20 + 2 * kStages, kNumBars = 21 + 2 * kStages;
+    // shared memory: Q_0, Q_1, dO_0, dO_1, then the ring
+    static constexpr int kDataBytes = 4 * kTileBytes + kStages * kTileBytes;
     static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 32 + 1024;
-    static constexpr int kColS = 0, kColDP = 128, kColDQ = 256;
+    static constexpr int kColDQ = 256;
 };
 
-// Key blocks query block i meets (causal: j <= i).
-__device__ __forceinline__ int q_nkv(const Params &p, int i) { return p.causal ? i + 1 : p.nblk; }
+// dq unit -> (b, h, m): m is a 256-row block; tile t covers rows m 256 + 128 t.
+struct QUnit2 {
+    int b, h, m;
+    int row0[2];
+    int nkv[2];  // 128-key blocks tile t visits (0: tile past N)
+    int nmax;
+};
+__device__ __forceinline__ QUnit2 q_unit2(const Params &p, long long u) {
+    QUnit2 w;
+    const int nq = (p.N + 2 * kRows - 1) / (2 * kRows);  // 256-row blocks per head
+    int r;
+    if (p.order == kBlockFirst) {
+        w.h = int(u % p.Hq);
+        const long long bm = u / p.Hq;
+        r = int(bm % nq);
+        w.b = int(bm / nq);
+    } else {
+        r = int(u % nq);
+        const long long bh = u / nq;
+        w.h = int(bh % p.Hq);
+        w.b = int(bh / p.Hq);
+    }
+    w.m = p.causal ? (nq - 1 - r) : r;
+    w.nmax = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int r0 = w.m * 2 * kRows + t * kRows;
+        w.row0[t] = r0;
+        int n = 0;
+        if (r0 < p.N) n = p.causal ? min(p.nblk, r0 / kRows + 1) : p.nblk;
+        w.nkv[t] = n;
+        w.nmax = max(w.nmax, n);
+    }
+    return w;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -682,9 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *sQ = smem;
-    uint8_t *sDO = smem + C::kTileBytes;
-    uint8_t *sStage = smem + 2 * C::kTileBytes;
+    uint8_t *sQ = smem;                         // two tiles
+    uint8_t *sDO = smem + 2 * C::kTileBytes;    // two tiles
+    uint8_t *sKV = smem + 4 * C::kTileBytes;    // ring
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kDataBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -693,20 +741,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     auto bar = [&](int i) { return smem_u32(bars + i); };
-    auto stage_k = [&](int s) { return sStage + s * C::kStageBytes; };
-    auto stage_v = [&](int s) { return sStage + s * C::kStageBytes + C::kTileBytes; };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::kBarQFull), 1);
-        mbar_init(bar(C::kBarQEmpty), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(C::kBarQFull + t), 1);
+            mbar_init(bar(C::kBarQEmpty + t), 1);
+            mbar_init(bar(C::kBarSFull + t), 1);
+            mbar_init(bar(C::kBarPFull + t), 4);
+            mbar_init(bar(C::kBarDPFull + t), 1);
+            mbar_init(bar(C::kBarDSFull + t), 4);
+            mbar_init(bar(C::kBarAccFull + t), 1);
+            mbar_init(bar(C::kBarAccEmpty + t), 4);
+        }
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(C::kBarKVFull + s), 1);
             mbar_init(bar(C::kBarKVEmpty + s), 1);
         }
-        mbar_init(bar(C::kBarSFull), 1);
-        mbar_init(bar(C::kBarPFull), kEwWarps);
-        mbar_init(bar(C::kBarAccFull), 1);
-        mbar_init(bar(C::kBarAccEmpty), kEwWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(C::kBarUQFull + i), 1);
             mbar_init(bar(C::kBarUQEmpty + i), 1 + kEwWarps);
@@ -737,8 +787,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             long long fills = 0;
-            int q_loads = 0;
+            int q_loads[2] = {0, 0};
             bool ok = true;
+            auto emit = [&](const CUtensorMap *map, int blk, int plane) {
+                const int slot = int(fills % C::kStages);
+                const long long round = fills / C::kStages;
+                if (round > 0 && !mbar_wait_bounded(bar(C::kBarKVEmpty + slot), uint32_t((round - 1) & 1),
+                                                    p.wait_ns, abort_flag, status))
+                    return false;
+                const uint32_t fb = bar(C::kBarKVFull + slot);
+                mbar_arrive_expect_tx(fb, C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(smem_u32(sKV + slot * C::kTileBytes + c * C::kChunkBytes), map, fb, c * 64,
+                                blk * kRows, plane);
+                ++fills;
+                return true;
+            };
             for (long long qi = 0; ok; ++qi) {
                 const long long u = fetch_unit(p, 1, qi);
                 const int qs = int(qi & 1);
@@ -750,37 +814,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 unit_q[qs] = int(u);
                 mbar_arrive(bar(C::kBarUQFull + qs));
                 if (u < 0) break;
-                const QUnit w = q_unit(p, u);
+                const QUnit2 w = q_unit2(p, u);
                 const int bh = w.b * p.Hq + w.h;
-                if (q_loads > 0 && !mbar_wait_bounded(bar(C::kBarQEmpty), uint32_t((q_loads - 1) & 1), p.wait_ns,
-                                                      abort_flag, status)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(bar(C::kBarQFull), 2 * C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(smem_u32(sQ + c * C::kChunkBytes), &tmQ, bar(C::kBarQFull), c * 64, w.i * kRows, bh);
-                    tma_load_3d(smem_u32(sDO + c * C::kChunkBytes), &tmDO, bar(C::kBarQFull), c * 64, w.i * kRows,
-                                bh);
-                }
-                ++q_loads;
-                const int kvh = w.b * p.Hkv + w.h / p.G;
-                const int nkv = q_nkv(p, w.i);
-                for (int j = 0; j < nkv; ++j) {
-                    const int slot = int(fills % C::kStages);
-                    const long long round = fills / C::kStages;
-                    if (round > 0 && !mbar_wait_bounded(bar(C::kBarKVEmpty + slot), uint32_t((round - 1) & 1),
-                                                        p.wait_ns, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = bar(C::kBarKVFull + slot);
-                    mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (w.nkv[t] == 0) continue;
+                    if (q_loads[t] > 0)
+                        ok = mbar_wait_bounded(bar(C::kBarQEmpty + t), uint32_t((q_loads[t] - 1) & 1), p.wait_ns,
+                                               abort_flag, status);
+                    if (!ok) break;
+                    const uint32_t qb = bar(C::kBarQFull + t);
+                    mbar_arrive_expect_tx(qb, 2 * C::kTileBytes);
                     for (int c = 0; c < C::kChunks; ++c) {
-                        tma_load_3d(smem_u32(stage_k(slot) + c * C::kChunkBytes), &tmK, fb, c * 64, j * kRows, kvh);
-                        tma_load_3d(smem_u32(stage_v(slot) + c * C::kChunkBytes), &tmV, fb, c * 64, j * kRows, kvh);
+                        tma_load_3d(smem_u32(sQ + t * C::kTileBytes + c * C::kChunkBytes), &tmQ, qb, c * 64,
+                                    w.row0[t], bh);
+                        tma_load_3d(smem_u32(sDO + t * C::kTileBytes + c * C::kChunkBytes), &tmDO, qb, c * 64,
+                                    w.row0[t], bh);
                     }
-                    ++fills;
+                    ++q_loads[t];
+                }
+                const int plane = w.b * p.Hkv + w.h / p.G;
+                for (int j = 0; ok && j < w.nmax; ++j) {
+                    ok = emit(&tmK, j, plane);
+                    if (ok) ok = emit(&tmV, j, plane);
                 }
             }
             if (!ok) {
@@ -793,21 +848,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            &no_abort, status))
                         atomicOr(status, kStatusDrainTimeout);
                 }
-                if (q_loads > 0 && !mbar_wait_bounded(bar(C::kBarQFull), uint32_t((q_loads - 1) & 1), drain_ns,
-                                                      &no_abort, status))
-                    atomicOr(status, kStatusDrainTimeout);
+                for (int t = 0; t < 2; ++t)
+                    if (q_loads[t] > 0 && !mbar_wait_bounded(bar(C::kBarQFull + t), uint32_t((q_loads[t] - 1) & 1),
+                                                             drain_ns, &no_abort, status))
+                        atomicOr(status, kStatusDrainTimeout);
             }
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kRows, kRows, 0);
             constexpr uint32_t kIdescAcc = idesc_bf16_f32(kRows, D, 1);
-            const uint64_t dQ0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t dO0 = smem_desc_sw128(smem_u32(sDO), 16, 1024);
             long long fills = 0;
-            int q_used = 0, p_waits = 0, units_done = 0;
+            int q_used[2] = {0, 0}, p_waits[2] = {0, 0}, ds_waits[2] = {0, 0}, units_done[2] = {0, 0};
             bool ok = true;
+            auto slot_of = [&](long long f) { return int(f % C::kStages); };
+            auto wait_fill = [&](long long f) {
+                return mbar_wait_bounded(bar(C::kBarKVFull + slot_of(f)), uint32_t((f / C::kStages) & 1), p.wait_ns,
+                                         abort_flag, status);
+            };
+            auto kmaj = [&](long long f) { return smem_desc_sw128(smem_u32(sKV + slot_of(f) * C::kTileBytes), 16, 1024); };
+            auto issue_s = [&](int t, long long fK) {  // S(t) = Q_t K^T -> X(t)
+                ss_product<D, C::kChunkBytes>(tmem_base + kRows * t,
+                                              smem_desc_sw128(smem_u32(sQ + t * C::kTileBytes), 16, 1024), kmaj(fK),
+                                              kIdescS);
+                tc_commit(bar(C::kBarSFull + t));
+            };
             for (long long qi = 0; ok; ++qi) {
                 const int qs = int(qi & 1);
                 ok = mbar_wait_bounded(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag,
@@ -816,43 +882,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const long long u = unit_q[qs];
                 mbar_arrive(bar(C::kBarUQEmpty + qs));
                 if (u < 0) break;
-                const QUnit w = q_unit(p, u);
-                const int nkv = q_nkv(p, w.i);
-                ok = mbar_wait_bounded(bar(C::kBarQFull), uint32_t(q_used & 1), p.wait_ns, abort_flag, status);
-                if (!ok) break;
-                ++q_used;
-                for (int j = 0; ok && j < nkv; ++j) {
-                    const int slot = int(fills % C::kStages);
-                    ok = mbar_wait_bounded(bar(C::kBarKVFull + slot), uint32_t((fills / C::kStages) & 1), p.wait_ns,
-                                           abort_flag, status);
+                const QUnit2 w = q_unit2(p, u);
+                const long long f0 = fills;  // K_j at f0 + 2 j, V_j at f0 + 2 j + 1
+                ok = wait_fill(f0);
+                for (int t = 0; ok && t < 2; ++t) {
+                    if (w.nkv[t] == 0) continue;
+                    ok = mbar_wait_bounded(bar(C::kBarQFull + t), uint32_t(q_used[t] & 1), p.wait_ns, abort_flag,
+                                           status);
                     if (!ok) break;
+                    ++q_used[t];
                     tc_fence_after();
-                    const uint64_t dKk = smem_desc_sw128(smem_u32(stage_k(slot)), 16, 1024);
-                    const uint64_t dVk = smem_desc_sw128(smem_u32(stage_v(slot)), 16, 1024);
-                    // S = Q K^T and dP = dO V^T
-                    ss_product<D, C::kChunkBytes>(tmem_base + C::kColS, dQ0, dKk, kIdescS);
-                    ss_product<D, C::kChunkBytes>(tmem_base + C::kColDP, dO0, dVk, kIdescS);
-                    tc_commit(bar(C::kBarSFull));
-                    ok = mbar_wait_bounded(bar(C::kBarPFull), uint32_t(p_waits & 1), p.wait_ns, abort_flag, status);
+                    issue_s(t, f0);
+                }
+                for (int j = 0; ok && j < w.nmax; ++j) {
+                    const long long fK = f0 + 2 * j, fV = fK + 1;
+                    // dP(t, j) once warpgroup t holds P (X(t) is free again)
+                    ok = wait_fill(fV);
+                    for (int t = 0; ok && t < 2; ++t) {
+                        if (j >= w.nkv[t]) continue;
+                        ok = mbar_wait_bounded(bar(C::kBarPFull + t), uint32_t(p_waits[t] & 1), p.wait_ns, abort_flag,
+                                               status);
+                        if (!ok) break;
+                        ++p_waits[t];
+                        tc_fence_after();
+                        ss_product<D, C::kChunkBytes>(tmem_base + kRows * t,
+                                                      smem_desc_sw128(smem_u32(sDO + t * C::kTileBytes), 16, 1024),
+                                                      kmaj(fV), kIdescS);
+                        tc_commit(bar(C::kBarDPFull + t));
+                    }
                     if (!ok) break;
-                    ++p_waits;
-                    if (j == 0 && units_done > 0) {
-                        ok = mbar_wait_bounded(bar(C::kBarAccEmpty), uint32_t((units_done - 1) & 1), p.wait_ns,
+                    tc_commit(bar(C::kBarKVEmpty + slot_of(fV)));  // V_j consumed
+                    // dQ(t, j) once warpgroup t wrote dS, then S(t, j + 1)
+                    bool k_next = false;
+                    for (int t = 0; ok && t < 2; ++t) {
+                        if (j >= w.nkv[t]) continue;
+                        ok = mbar_wait_bounded(bar(C::kBarDSFull + t), uint32_t(ds_waits[t] & 1), p.wait_ns,
                                                abort_flag, status);
                         if (!ok) break;
+                        ++ds_waits[t];
+                        if (j == 0 && units_done[t] > 0) {
+                            ok = mbar_wait_bounded(bar(C::kBarAccEmpty + t), uint32_t((units_done[t] - 1) & 1),
+                                                   p.wait_ns, abort_flag, status);
+                            if (!ok) break;
+                        }
+                        tc_fence_after();
+                        const uint64_t kmn = smem_desc_sw128(smem_u32(sKV + slot_of(fK) * C::kTileBytes), C::kChunkBytes,
+                                                             1024);
+                        ts_product<8>(tmem_base + C::kColDQ + D * t, tmem_base + kRows * t, kmn, kIdescAcc, j > 0);
+                        if (j + 1 < w.nkv[t]) {
+                            if (!k_next) {
+                                ok = wait_fill(fK + 2);
+                                if (!ok) break;
+                                k_next = true;
+                                tc_fence_after();
+                            }
+                            issue_s(t, fK + 2);
+                        } else {
+                            tc_commit(bar(C::kBarAccFull + t));  // dQ(t) final for this unit
+                            tc_commit(bar(C::kBarQEmpty + t));   // Q_t, dO_t reusable
+                            ++units_done[t];
+                        }
                     }
-                    tc_fence_after();
-                    // dQ += dS K (dS bf16 in TMEM over S; K read MN-major)
-                    const uint64_t dKmn = smem_desc_sw128(smem_u32(stage_k(slot)), C::kChunkBytes, 1024);
-                    ts_product<8>(tmem_base + C::kColDQ, tmem_base + C::kColS + kPackOff, dKmn, kIdescAcc, j > 0);
-                    tc_commit(bar(C::kBarKVEmpty + slot));
-                    ++fills;
-                    if (j == nkv - 1) {
-                        tc_commit(bar(C::kBarAccFull));
-                        tc_commit(bar(C::kBarQEmpty));
-                        ++units_done;
-                    }
+                    if (!ok) break;
+                    tc_commit(bar(C::kBarKVEmpty + slot_of(fK)));  // K_j consumed
                 }
+                fills = f0 + 2 * (long long)w.nmax;
             }
             tc_commit(bar(C::kBarDrain));
             volatile int no_abort = 0;
@@ -864,18 +958,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEwRegs));
         // ---------------------------------------------------------------- elementwise / epilogue
-        // Two warps per TMEM lane quarter: warp w reads query rows
-        // [32 (w % 4), +32) and the key columns [64 h, 64 h + 64),
-        // h = (w - 4) / 4.  dS (bf16) goes to columns [32, 96) of S, so each
-        // warp overwrites only columns that it has already read.
+        // Warpgroup t = (w - 4) / 4 owns tile t; warp w reads TMEM lanes
+        // [32 (w % 4), +32), one query row per thread.
+        const int t = (warp - 4) >> 2;
         const int quarter = warp & 3;
-        const int half = (warp - 4) >> 2;
-        const int r = quarter * 32 + lane;  // query row inside the block
+        const int r = quarter * 32 + lane;
         const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-        const uint32_t tS = tmem_base + lane_off + C::kColS;
-        const uint32_t tDP = tmem_base + lane_off + C::kColDP;
+        const uint32_t tX = tmem_base + lane_off + kRows * t;
         const float sl2 = p.scale_log2;
-        int s_waits = 0, acc_waits = 0;
+        int s_waits = 0, dp_waits = 0, acc_waits = 0;
         bool ok = true;
         for (long long qi = 0; ok; ++qi) {
             const int qs = int(qi & 1);
@@ -885,63 +976,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarUQEmpty + qs));
             if (u < 0) break;
-            const QUnit w = q_unit(p, u);
-            const int nkv = q_nkv(p, w.i);
-            const int row = w.i * kRows + r;
+            const QUnit2 w = q_unit2(p, u);
+            const int nkv = w.nkv[t];
+            if (nkv == 0) continue;
+            const int row = w.row0[t] + r;
             const size_t prow = (size_t)(w.b * p.Hq + w.h) * p.npad + row;  // row < npad always
             const float neg_l = -p.lse2[prow];                               // -inf past N
             const float del = p.delta[prow];
             for (int j = 0; j < nkv; ++j) {
-                ok = mbar_wait_warp(bar(C::kBarSFull), uint32_t(s_waits & 1), p.wait_ns, abort_flag, status);
+                // P = exp(S - lse), kept in registers
+                ok = mbar_wait_warp(bar(C::kBarSFull + t), uint32_t(s_waits & 1), p.wait_ns, abort_flag, status);
                 if (!ok) break;
                 ++s_waits;
                 tc_fence_after();
-                // Both chunks of this warp's half are read before anything is
-                // written (the first chunk's bf16 lands on the second's columns).
-                uint32_t sv[2][32], dv[2][32];
+                float pr[kRows];
+                {
+                    uint32_t sv[4][32];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_ld32(tS + (2 * half + c) * 32, sv[c]);
-                    tmem_ld32(tDP + (2 * half + c) * 32, dv[c]);
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tX + c * 32, sv[c]);
+                    tmem_wait_ld();
+                    const int kv0 = j * kRows;
+                    int lim = kRows;  // block columns c >= lim are masked (past N or after the row)
+                    if (kv0 + kRows > p.N) lim = p.N - kv0;
+                    if (p.causal && j == w.row0[t] / kRows) lim = min(lim, r + 1);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            float x0, x1;
+                            ffma2(x0, x1, __uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1]), sl2, sl2,
+                                  neg_l, neg_l);
+                            const int k = c * 32 + 2 * e;
+                            pr[k] = k < lim ? fast_exp2(x0) : 0.f;
+                            pr[k + 1] = k + 1 < lim ? fast_exp2(x1) : 0.f;
+                        }
                 }
-                const int kv0 = j * kRows;
-                int lim = kRows;  // block columns c >= lim are masked (past N or after the row)
-                if (kv0 + kRows > p.N) lim = p.N - kv0;
-                if (p.causal && j == w.i) lim = min(lim, r + 1);
-                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarPFull + t));
+                // dS = P (dP - Delta) -> bf16 over the first 64 columns of X(t)
+                ok = mbar_wait_warp(bar(C::kBarDPFull + t), uint32_t(dp_waits & 1), p.wait_ns, abort_flag, status);
+                if (!ok) break;
+                ++dp_waits;
+                tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int k0 = (2 * half + c) * 32;  // first block column of the chunk
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t dv[32];
+                    tmem_ld32(tX + c * 32, dv);
+                    tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float x0, x1;
-                        ffma2(x0, x1, __uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1]), sl2, sl2,
-                              neg_l, neg_l);
-                        float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                        if (k0 + 2 * e >= lim) p0 = 0.f;
-                        if (k0 + 2 * e + 1 >= lim) p1 = 0.f;
-                        pk[e] = pack_bf16x2(p0 * (__uint_as_float(dv[c][2 * e]) - del),
-                                            p1 * (__uint_as_float(dv[c][2 * e + 1]) - del));
-                    }
-                    tmem_st16(tS + kPackOff + k0 / 2, pk);
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(pr[c * 32 + 2 * e] * (__uint_as_float(dv[2 * e]) - del),
+                                            pr[c * 32 + 2 * e + 1] * (__uint_as_float(dv[2 * e + 1]) - del));
+                    tmem_st16(tX + c * 16, pk);  // over columns already read
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::kBarPFull));
+                if (lane == 0) mbar_arrive(bar(C::kBarDSFull + t));
             }
             if (!ok) break;
-            ok = mbar_wait_warp(bar(C::kBarAccFull), uint32_t(acc_waits & 1), p.wait_ns, abort_flag, status);
+            ok = mbar_wait_warp(bar(C::kBarAccFull + t), uint32_t(acc_waits & 1), p.wait_ns, abort_flag, status);
             if (!ok) break;
             ++acc_waits;
             tc_fence_after();
             const bool row_ok = row < p.N;
             const size_t off = ((size_t)(w.b * p.Hq + w.h) * p.N + (row_ok ? row : 0)) * p.d_store;
-            store_half_row<D>(tmem_base + lane_off + C::kColDQ, half, p.out0 + off, row_ok, p.d_store, p.scale);
+            store_half_row<D>(tmem_base + lane_off + C::kColDQ + D * t, 0, p.out0 + off, row_ok, p.d_store, p.scale);
+            store_half_row<D>(tmem_base + lane_off + C::kColDQ + D * t, 1, p.out0 + off, row_ok, p.d_store, p.scale);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarAccEmpty));
+            if (lane == 0) mbar_arrive(bar(C::kBarAccEmpty + t));
         }
     }
 
@@ -1036,7 +1142,7 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
     // dQ
     p.out0 = reinterpret_cast<__nv_bfloat16 *>(a.dq);
     p.out1 = nullptr;
-    p.total_units = (long long)a.B * a.Hq * nblk;
+    p.total_units = (long long)a.B * a.Hq * ((a.N + 2 * kRows - 1) / (2 * kRows));  // 256-row units
     grid = p.total_units;
     if (a.order != kNaiveHeadFirst && grid > a.num_sms) grid = a.num_sms;
     if (grid > 0x7fffffffLL) return -2;
