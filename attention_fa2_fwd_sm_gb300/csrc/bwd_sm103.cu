@@ -74,11 +74,6 @@ constexpr int kLaunchRegs = 168;
 constexpr int kCtrlRegs = 128;
 constexpr int kEwRegs = 184;
 static_assert(128 * kCtrlRegs + 256 * kEwRegs <= kThreads * kLaunchRegs, "register split");
-// dq pass: bf16 dS of the 128-column fp32 S tile is written at column offset
-// 32 of it (64 columns), so a warp only overwrites columns that it has
-// already read: the warp on columns [0, 64) writes [32, 64), the one on
-// [64, 128) writes [64, 96).
-constexpr int kPackOff = 32;
 
 struct Params {
     __nv_bfloat16 *out0, *out1;  // dkdv: dK, dV; dq: dQ (out1 unused)
@@ -153,29 +148,6 @@ __device__ __forceinline__ KvUnit kv_unit(const Params &p, long long u) {
         w.g = int(bg % p.Hkv);
         w.b = int(bg / p.Hkv);
     }
-    return w;
-}
-
-// dq unit -> (b, query head h, query block i): the forward pass's unit map
-// with 128-row blocks (causal: descending i, longest first).
-struct QUnit {
-    int b, h, i;
-};
-__device__ __forceinline__ QUnit q_unit(const Params &p, long long u) {
-    QUnit w;
-    int r;
-    if (p.order == kBlockFirst) {
-        w.h = int(u % p.Hq);
-        const long long bm = u / p.Hq;
-        r = int(bm % p.nblk);
-        w.b = int(bm / p.nblk);
-    } else {
-        r = int(u % p.nblk);
-        const long long bh = u / p.nblk;
-        w.h = int(bh % p.Hq);
-        w.b = int(bh / p.Hq);
-    }
-    w.i = p.causal ? (p.nblk - 1 - r) : r;
     return w;
 }
 
