@@ -25,9 +25,12 @@
 // over S in TMEM and O += P V is a TS MMA with V read MN-major from shared
 // memory.  The issue order QK(t, j+1) after PV(t, j) means the commit that
 // announces S(t, j+1) also guarantees PV(t, j) is complete, so the softmax
-// warps may rescale O(t) in TMEM right after they see S(t, j+1); O is only
-// rescaled when a row's maximum grows by more than 2^8 (exactly the same
-// result up to rounding, since l and O always share the reference maximum).
+// warps may rescale O(t) in TMEM right after they see S(t, j+1).  The row's
+// reference maximum is exact for its first block and then kept while the
+// block's exponentials sum below 2^60 (no overflow is possible there); only
+// when that check fails is the block maximum taken, O rescaled and P
+// rewritten (the same result up to rounding, since l and O always share the
+// reference maximum).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -68,7 +71,6 @@ constexpr int kCtrlRegs = 104;
 constexpr int kSoftmaxRegs = 192;
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kTmemCols = 512;
-constexpr float kRescaleLog2 = 8.0f;  // lazy O rescale threshold (log2 units)
 
 template <int D>
 struct Cfg {
@@ -484,44 +486,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 128; ++c)
                         if (c >= lim) s[c] = -INFINITY;
                 }
-                // Row maximum: four independent chains of three-input maxima.
-                float mq[4];
+                // Row maximum of the block: four independent chains of three-input maxima.
+                auto block_max = [&]() {
+                    float mq[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float m = fmax3(s[32 * c], s[32 * c + 1], s[32 * c + 2]);
+                    for (int c = 0; c < 4; ++c) {
+                        float m = fmax3(s[32 * c], s[32 * c + 1], s[32 * c + 2]);
 #pragma unroll
-                    for (int i = 3; i < 31; i += 2) m = fmax3(m, s[32 * c + i], s[32 * c + i + 1]);
-                    mq[c] = fmaxf(m, s[32 * c + 31]);
-                }
-                const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-                const float m_new = fmaxf(m_run, mx * sl2);
-                float corr = 1.f;
-                if (m_new > m_run + kRescaleLog2) {
-                    corr = fast_exp2(m_run - m_new);  // 0 when m_run = -inf
-                    m_run = m_new;
-                }
-                l_run *= corr;
-                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-
-                // P = 2^(s*scale*log2e - m) in bf16, written over S in TMEM; the
-                // row sum goes to four independent pairs of partial sums.
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x0, x1;
-                        ffma2(x0, x1, s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1], sl2, sl2, neg_m, neg_m);
-                        const float p0 = fast_exp2(x0);
-                        const float p1 = fast_exp2(x1);
-                        const int a = (i & 3) * 2;
-                        fadd2(ls[a], ls[a + 1], p0, p1);
-                        pk[i] = pack_bf16x2(p0, p1);
+                        for (int i = 3; i < 31; i += 2) m = fmax3(m, s[32 * c + i], s[32 * c + i + 1]);
+                        mq[c] = fmaxf(m, s[32 * c + 31]);
                     }
-                    tmem_st16(tS + c * 16, pk);
+                    return fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+                };
+                // P = 2^(s*scale*log2e - m) in bf16, written over S in TMEM; returns
+                // the block's row sum (four independent pairs of partial sums).
+                auto exp_block = [&](float neg_m) {
+                    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float x0, x1;
+                            ffma2(x0, x1, s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1], sl2, sl2, neg_m, neg_m);
+                            const float p0 = fast_exp2(x0);
+                            const float p1 = fast_exp2(x1);
+                            const int a = (i & 3) * 2;
+                            fadd2(ls[a], ls[a + 1], p0, p1);
+                            pk[i] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(tS + c * 16, pk);
+                    }
+                    return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                };
+                // The reference maximum m_run is exact for a row's first block and
+                // is otherwise kept: exponentials against it cannot overflow while
+                // the block's sum stays below 2^60 (bf16 and fp32 share the
+                // exponent range), so the block maximum is only needed when that
+                // check fails.  Then the warp takes the exact maximum, rescales and
+                // writes P again (lanes whose reference did not move store the
+                // same values once more).
+                float corr = 1.f;
+                if (m_run == -INFINITY) m_run = block_max() * sl2;  // stays -inf if all masked
+                float l_blk = exp_block(m_run == -INFINITY ? 0.f : -m_run);
+                if (__any_sync(0xffffffffu, !(l_blk < 0x1p60f))) {
+                    const float m_new = fmaxf(m_run, block_max() * sl2);
+                    if (m_new > m_run) {
+                        corr = fast_exp2(m_run - m_new);
+                        m_run = m_new;
+                    }
+                    tmem_wait_st();
+                    l_blk = exp_block(m_run == -INFINITY ? 0.f : -m_run);
                 }
-                l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                l_run = l_run * corr + l_blk;
                 // Rescale this row of O when its reference maximum moved (never on
                 // the first block: PV(t, 0) overwrites O).
                 if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
