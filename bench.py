@@ -40,10 +40,10 @@ DEC = dict(B=8, Hq=64, Hkv=8, S=32768, d=128)
 # digest; after any change to them the bench reports null until re-captured.
 MEASURED_TRAFFIC = {
     "fwd": {"files": ["fwd_sm103.cu", "sm103_ptx.cuh", "tile_order.cuh"],
-            "sha256": "f85c8ae35f9709b87d0834934a0cb91a11d696fef83048d36c9ced6cded9c49b",
+            "sha256": "9229ea21e4cd0e235680fd0abfec9ea90e2dcbfaa290c4c59582b72d6fa9c160",
             # MHA B=1 H=128 d=128, head-first, captured at N=32768 and N=8192 (one-pass
             # capture of dram__bytes_read.sum + dram__bytes_write.sum)
-            "bytes_by_n": {32768: 3233039104 + 1088919296, 8192: 805848576 + 251660032}},
+            "bytes_by_n": {32768: 3232415488 + 1087872512, 8192: 806408960 + 251140864}},
     "decode": {"files": ["decode_sm103.cu", "sm103_ptx.cuh"],
                "sha256": "84c5c7a81f5fab826c433a44b2424358cd61441d6fd4f7a86ee0e3df18b4451c",
                # GQA decode B=8 Hq=64 Hkv=8 d=128, 4 splits, captured at 8192 keys;
