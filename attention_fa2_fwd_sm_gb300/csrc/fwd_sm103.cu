@@ -381,7 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     issue_qk(t, f0);
                     tc_commit(bar(C::kBarSFull + t));
-                    if (t == last_user(w, 0)) tc_commit(bar(C::kBarKVEmpty + int(f0 % C::kStages)));
                 }
                 for (int j = 0; ok && j < w.nmax; ++j) {
                     const long long fV = f0 + 2 * j + 1, fK = f0 + 2 * j + 2;
@@ -413,8 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             issue_qk(t, fK);
                             tc_commit(bar(C::kBarSFull + t));
-                            if (t == last_user(w, j + 1))
-                                tc_commit(bar(C::kBarKVEmpty + int(fK % C::kStages)));
                         } else {
                             tc_commit(bar(C::kBarOFull + t));   // O(t) final for this unit
                             tc_commit(bar(C::kBarQEmpty + t));  // Q(t) buffer reusable
@@ -443,6 +440,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem_base + lane_off + C::kOCol + t * D;
         const float sl2 = p.scale_log2;
         int s_waits = 0, o_waits = 0;
+        long long kv_base = 0;  // ring position of the current unit's first K/V fill
+        // One thread of the warpgroup frees K slots of the ring.  S(t, j)
+        // complete means every MMA issued before its commit is complete, QK(t', j)
+        // of every tile included, so the last tile to use K_j frees its slot on
+        // seeing S(t, j) and the MMA thread needs no commit of its own for it.
+        // (V slots keep their commit right after the last PV that reads them:
+        // waiting for the next S would free them about eight MMAs later, which
+        // measured slower.)
+        const bool frees_slots = (quarter == 0 && lane == 0);
         bool ok = true;
 
         for (long long qi = 0; ok; ++qi) {
@@ -455,6 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(C::kBarUQEmpty + qs));
             if (u < 0) break;
             const UnitWork w = unit_work(p, u);
+            const long long f0 = kv_base;  // K_j at ring position f0 + 2j
+            kv_base += 2 * (long long)w.nmax;
             const int nkv = w.nkv[t];
             if (nkv == 0) continue;
             const int row = w.row0[t] + r;
@@ -465,6 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     status);
                 if (!ok) break;
                 ++s_waits;
+                if (frees_slots && t == last_user(w, j))
+                    mbar_arrive(bar(C::kBarKVEmpty + int((f0 + 2 * j) % C::kStages)));
                 tc_fence_after();
                 uint32_t sr[4][32];
 #pragma unroll
