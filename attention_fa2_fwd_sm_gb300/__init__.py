@@ -41,6 +41,8 @@ _FP = ctypes.POINTER(ctypes.c_float)
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ, _P]),
+    "attn_fwd_host_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
@@ -122,6 +124,17 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, stream=None) -> i
 def attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, stream=None) -> int:
     return lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
                              float(scale), int(bool(causal)), int(tile_order), _stream(stream))
+
+
+def attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, kv_heads_per_chunk,
+                  workspace, workspace_bytes, stream=None) -> int:
+    return lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
+                               int(bool(causal)), int(tile_order), int(kv_heads_per_chunk), _ptr(workspace),
+                               int(workspace_bytes), _stream(stream))
+
+
+def attn_fwd_host_workspace_bytes(B, Hq, Hkv, N, d, kv_heads_per_chunk=0) -> int:
+    return int(lib().attn_fwd_host_workspace_bytes(B, Hq, Hkv, N, d, kv_heads_per_chunk))
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, tile_order,
@@ -254,6 +267,34 @@ def forward(q, k, v, causal=False, scale=None, tile_order=ORDER_HEAD_FIRST, with
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if with_lse else None
     check(attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, stream),
           "attn_fwd_ex")
+    return o, lse
+
+
+def forward_host(q, k, v, causal=False, scale=None, tile_order=ORDER_HEAD_FIRST, with_lse=True,
+                 kv_heads_per_chunk=0, workspace=None, out=None, device=None, stream=None, synchronize=True):
+    """Run attn_fwd_host on ``[B, H, N, d]`` bf16 CPU tensors (pinned for overlap).
+
+    Allocates pinned outputs (unless ``out = (o, lse)`` is given) and a device
+    workspace (unless given); with ``synchronize`` it waits for the stream, so
+    the outputs are ready on return.  Returns ``(o, lse)``."""
+    import torch
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    nbytes = attn_fwd_host_workspace_bytes(B, Hq, Hkv, N, d, kv_heads_per_chunk)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    if out is None:
+        o = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=True) if with_lse else None
+    else:
+        o, lse = out
+    check(attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, kv_heads_per_chunk,
+                        workspace, nbytes, stream), "attn_fwd_host")
+    if synchronize:
+        torch.cuda.current_stream(dev).synchronize() if stream is None else torch.cuda.synchronize(dev)
     return o, lse
 
 

@@ -145,10 +145,7 @@ int attn_die_map(int *die_of_sm, int capacity, float *stats) {
     return die_map_query(die_of_sm, capacity, stats);
 }
 
-static int validate_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                        int Hq, int Hkv, int N, int d, float scale, int tile_order) {
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_ARG;
-    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_ARG;
+static int validate_fwd_sizes(int B, int Hq, int Hkv, int N, int d, float scale, int tile_order) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0) return ATTN_ERR_ARG;
     if (Hq % Hkv) return ATTN_ERR_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_ARG;
@@ -159,19 +156,19 @@ static int validate_fwd(const void *q, const void *k, const void *v, void *o, fl
     return ATTN_OK;
 }
 
-int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
-                int Hkv, int N, int d, float scale, int causal, int tile_order,
-                attn_stream_t stream) {
-    int rc = validate_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, tile_order);
-    if (rc != ATTN_OK) return rc;
-    const int sms = current_num_sms();
-    if (sms <= 0) return note_cuda_error(cudaErrorNoDevice, "device query");
+static int validate_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                        int Hq, int Hkv, int N, int d, float scale, int tile_order) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_ARG;
+    return validate_fwd_sizes(B, Hq, Hkv, N, d, scale, tile_order);
+}
+
+static FwdLaunch fwd_problem(int B, int Hq, int Hkv, int N, int d, float scale, int causal, int tile_order,
+                             int sms) {
     FwdLaunch a;
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.o = o;
-    a.lse = lse;
+    a.q = a.k = a.v = nullptr;
+    a.o = nullptr;
+    a.lse = nullptr;
     a.B = B;
     a.Hq = Hq;
     a.Hkv = Hkv;
@@ -182,7 +179,55 @@ int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
     a.order = tile_order;
     a.wait_ns = (unsigned long long)g_wait_ns.load();
     a.num_sms = sms;
+    return a;
+}
+
+int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                int Hkv, int N, int d, float scale, int causal, int tile_order,
+                attn_stream_t stream) {
+    int rc = validate_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, tile_order);
+    if (rc != ATTN_OK) return rc;
+    const int sms = current_num_sms();
+    if (sms <= 0) return note_cuda_error(cudaErrorNoDevice, "device query");
+    FwdLaunch a = fwd_problem(B, Hq, Hkv, N, d, scale, causal, tile_order, sms);
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
     return fwd_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int kv_heads_per_chunk) {
+    if (validate_fwd_sizes(B, Hq, Hkv, N, d, 1.f, kHeadFirst) != ATTN_OK) return 0;
+    if (kv_heads_per_chunk > Hkv) return 0;
+    const int gc = kv_heads_per_chunk > 0 ? kv_heads_per_chunk : host_default_chunk(Hq, Hkv, N);
+    return 2 * host_chunk_layout(Hq, Hkv, N, d, gc).slot_bytes;
+}
+
+int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
+                  int N, int d, float scale, int causal, int tile_order, int kv_heads_per_chunk,
+                  void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_ARG;
+    int rc = validate_fwd_sizes(B, Hq, Hkv, N, d, scale, tile_order);
+    if (rc != ATTN_OK) return rc;
+    if (kv_heads_per_chunk > Hkv) return ATTN_ERR_ARG;
+    const int gc = kv_heads_per_chunk > 0 ? kv_heads_per_chunk : host_default_chunk(Hq, Hkv, N);
+    const size_t need = 2 * host_chunk_layout(Hq, Hkv, N, d, gc).slot_bytes;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    const int sms = current_num_sms();
+    if (sms <= 0) return note_cuda_error(cudaErrorNoDevice, "device query");
+    FwdHostLaunch a;
+    a.fwd = fwd_problem(B, Hq, Hkv, N, d, scale, causal, tile_order, sms);
+    a.q_host = q;
+    a.k_host = k;
+    a.v_host = v;
+    a.o_host = o;
+    a.lse_host = lse;
+    a.kv_heads_per_chunk = gc;
+    a.workspace = workspace;
+    return fwd_host_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,

@@ -47,6 +47,28 @@ struct DecodeLaunch {
     int varlen_min_chunk = 0;
 };
 
+// Forward on host-resident tensors (fwd_host.cu): `fwd` holds the problem
+// (its q, k, v, o, lse pointers are unused), the rest the host buffers, the
+// chunk size in KV heads and the device workspace of two chunk slots.
+struct FwdHostLaunch {
+    FwdLaunch fwd;
+    const void *q_host, *k_host, *v_host;
+    void *o_host;
+    float *lse_host;  // may be null
+    int kv_heads_per_chunk;
+    void *workspace;
+};
+
+// Byte offsets of one workspace slot (one chunk of kv_heads_per_chunk KV
+// heads and their query heads): q, k, v, o (bf16) and lse (fp32), each
+// starting on a 256-byte boundary.
+struct HostChunkLayout {
+    size_t q_off, k_off, v_off, o_off, lse_off, slot_bytes;
+};
+HostChunkLayout host_chunk_layout(int Hq, int Hkv, int N, int d, int kv_heads_per_chunk);
+int host_default_chunk(int Hq, int Hkv, int N);
+int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream);
+
 // Record a failed CUDA call for attn_last_error() (this thread) and return
 // ATTN_ERR_CUDA.
 int note_cuda_error(cudaError_t e, const char *where);

@@ -102,6 +102,45 @@ int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
                 int tile_order, attn_stream_t stream);
 
 /*
+ * attn_fwd_ex on HOST-resident tensors, for callers whose q, k, v live in host
+ * memory: the copies to the device, the forward kernels and the copies of o
+ * and lse back are overlapped.  The problem is cut into chunks of
+ * kv_heads_per_chunk KV heads of one batch entry (each with the Hq / Hkv
+ * query heads that read them); while chunk c is computed, chunk c+1 is
+ * copied in and chunk c-1 copied out.  Results are bit-identical to attn_fwd_ex
+ * on device copies of the same tensors.
+ *   q, k, v, o, lse  HOST pointers with the layouts of attn_fwd (lse may be
+ *                    NULL).  Page-locked (pinned) memory lets the copies
+ *                    overlap the kernels; with pageable memory the result
+ *                    is the same but the copies do not overlap.
+ *   kv_heads_per_chunk  1..Hkv, or <= 0 for the library's choice: the
+ *                    fewest KV heads whose chunk holds at least 304 forward
+ *                    work units (two waves on 152 SMs; a unit is 256 query
+ *                    rows of one query head), at most Hkv.
+ *   workspace        DEVICE memory, 16-byte aligned, of at least
+ *                    attn_fwd_host_workspace_bytes(B, Hq, Hkv, N, d,
+ *                    kv_heads_per_chunk) bytes: two chunk slots of q, k, v,
+ *                    o and lse.
+ * Ordering: everything starts after the work already enqueued on `stream`,
+ * and work enqueued on `stream` after the call starts after the last copy
+ * back.  The call returns once the work is enqueued; the host buffers must
+ * stay valid, and o / lse unread, until `stream` has been synchronised.
+ * Internally the library uses three more streams and a few events per
+ * device (created on the first call); calls from several host threads are
+ * enqueued one after the other.  Other arguments and errors as attn_fwd_ex;
+ * ATTN_ERR_WORKSPACE if the workspace is missing, misaligned or too small.
+ */
+int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                  int tile_order, int kv_heads_per_chunk, void *workspace,
+                  size_t workspace_bytes, attn_stream_t stream);
+
+/* Device workspace bytes attn_fwd_host needs (0 for invalid sizes or a
+ * chunk larger than Hkv). */
+size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d,
+                                     int kv_heads_per_chunk);
+
+/*
  * Backward pass of attn_fwd: gradients dQ, dK, dV for the output gradient
  * dout.  The pages measure an FA2 backward pass under the same tile orders
  * (detail page, section 5 "backward pass"); the gradient itself is the chain

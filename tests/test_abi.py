@@ -218,3 +218,48 @@ def _dvl(**kw):
 ])
 def test_varlen_decode_argument_errors(L, kw, code):
     assert _dvl(**kw) == code
+
+
+def _fh(**kw):
+    a = dict(q=A16, k=A16, v=A16, o=A16, lse=None, B=1, Hq=4, Hkv=2, N=100, d=64, scale=0.1, causal=0, order=0,
+             chunk=0, ws=A16, ws_bytes=1 << 30, stream=0)
+    a.update(kw)
+    return attn.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"], a["d"],
+                              a["scale"], a["causal"], a["order"], a["chunk"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_ARG),
+    (dict(o=None), attn.ATTN_ERR_ARG),
+    (dict(lse=A16 + 2), attn.ATTN_ERR_ARG),
+    (dict(B=0), attn.ATTN_ERR_ARG),
+    (dict(Hq=3), attn.ATTN_ERR_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_ARG),
+    (dict(order=4), attn.ATTN_ERR_ARG),
+    (dict(chunk=3), attn.ATTN_ERR_ARG),  # more KV heads than Hkv
+    (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(ws=None), attn.ATTN_ERR_WORKSPACE),
+    (dict(ws=A16 + 8), attn.ATTN_ERR_WORKSPACE),
+    (dict(chunk=1, ws_bytes=2 * (2 * 25600 + 2 * 12800 + 1024) - 1), attn.ATTN_ERR_WORKSPACE),
+])
+def test_host_forward_argument_errors(L, kw, code):
+    """Host-buffer forward: host pointers need no alignment, but every other
+    check runs before any CUDA call, as for the device entry points."""
+    assert _fh(**kw) == code
+
+
+def test_host_forward_workspace_size(L):
+    # one slot: q, k, v, o (bf16) and lse (fp32) of one chunk, each rounded up to 256 bytes; two slots
+    def slot(gc, G, N, d):
+        r = lambda x: (x + 255) // 256 * 256
+        q, kv, l = gc * G * N * d * 2, gc * N * d * 2, gc * G * N * 4
+        return r(q) + 2 * r(kv) + r(q) + r(l)
+    assert attn.attn_fwd_host_workspace_bytes(1, 4, 2, 100, 56, 1) == 2 * slot(1, 2, 100, 56)
+    assert attn.attn_fwd_host_workspace_bytes(1, 4, 2, 100, 64, 2) == 2 * slot(2, 2, 100, 64)
+    # default chunk: the fewest KV heads holding 304 work units of 256 query rows, at most Hkv
+    assert attn.attn_fwd_host_workspace_bytes(1, 128, 128, 32768, 128, 0) == 2 * slot(3, 1, 32768, 128)
+    assert attn.attn_fwd_host_workspace_bytes(1, 128, 128, 1024, 128, 0) == 2 * slot(76, 1, 1024, 128)
+    assert attn.attn_fwd_host_workspace_bytes(8, 64, 8, 32768, 128, 0) == 2 * slot(1, 8, 32768, 128)
+    assert attn.attn_fwd_host_workspace_bytes(1, 64, 8, 512, 128, 0) == 2 * slot(8, 8, 512, 128)
+    assert attn.attn_fwd_host_workspace_bytes(1, 4, 2, 100, 64, 3) == 0
+    assert attn.attn_fwd_host_workspace_bytes(1, 4, 2, 100, 32, 1) == 0

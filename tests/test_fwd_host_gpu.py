@@ -1,0 +1,105 @@
+"""GPU checks of attn_fwd_host, the forward on host-resident tensors whose
+copies and kernels overlap in chunks of KV heads: its outputs are bit for bit
+those of attn_fwd_ex on device copies of the same inputs (every chunk is an
+independent forward problem), for several chunk sizes including a ragged last
+chunk, pinned and pageable host memory, GQA, causal and d = 56; and they match
+the fp64 oracle."""
+import pytest
+import torch
+
+import oracle
+from synthetic_inputs import prefill_inputs
+from tests.gpu_util import assert_close, scale_of, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def attn():
+    from attention_fa2_fwd_sm_gb300 import _build
+    _build.build()
+    import attention_fa2_fwd_sm_gb300 as A
+    A.lib()
+    oracle.build()
+    return A
+
+
+def _host(t, pinned):
+    h = t.cpu()
+    return h.pin_memory() if pinned else h.clone()
+
+
+CASES = [
+    # B, Hq, Hkv, N, d, causal, kv heads per chunk, pinned
+    (2, 8, 2, 300, 128, True, 0, True),
+    (2, 8, 2, 300, 128, True, 1, True),
+    (2, 8, 2, 300, 128, False, 2, False),
+    (1, 6, 6, 1000, 64, False, 4, True),   # chunks of 4 and 2 KV heads
+    (1, 6, 6, 1000, 64, True, 5, False),
+    (1, 4, 4, 513, 56, True, 3, True),
+    (3, 4, 1, 129, 128, False, 0, True),   # one KV head per batch entry: one chunk each
+    (1, 2, 2, 1, 64, False, 1, True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal,chunk,pinned", CASES)
+def test_host_forward_is_bit_identical_to_the_device_call(attn, B, Hq, Hkv, N, d, causal, chunk, pinned):
+    dev = torch.device("cuda")
+    q, k, v = prefill_inputs(3, B, Hq, Hkv, N, d, dev)
+    scale = scale_of(d)
+    o_dev, lse_dev = attn.forward(q, k, v, causal=causal, scale=scale)
+    hq, hk, hv = (_host(t, pinned) for t in (q, k, v))
+    o_h = torch.full(q.shape, float("nan"), dtype=q.dtype)
+    lse_h = torch.full((B, Hq, N), float("nan"), dtype=torch.float32)
+    if pinned:
+        o_h, lse_h = o_h.pin_memory(), lse_h.pin_memory()
+    o, lse = attn.forward_host(hq, hk, hv, causal=causal, scale=scale, kv_heads_per_chunk=chunk,
+                               out=(o_h, lse_h))
+    attn.check(attn.attn_device_status(), "device status")
+    assert torch.equal(o.view(torch.int16), o_dev.cpu().view(torch.int16))
+    assert torch.equal(lse, lse_dev.cpu())
+
+
+def test_host_forward_matches_the_oracle_and_repeats(attn):
+    """Two calls in a row on one workspace with different inputs, the second
+    without lse: each result against the oracle."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N, d = 1, 8, 2, 700, 128
+    scale = scale_of(d)
+    ws = torch.empty(attn.attn_fwd_host_workspace_bytes(B, Hq, Hkv, N, d, 1), dtype=torch.uint8, device=dev)
+    for seed, causal, with_lse in ((5, True, True), (6, False, False)):
+        q, k, v = (t.cpu().pin_memory() for t in prefill_inputs(seed, B, Hq, Hkv, N, d, dev))
+        o, lse = attn.forward_host(q, k, v, causal=causal, scale=scale, with_lse=with_lse,
+                                   kv_heads_per_chunk=1, workspace=ws)
+        attn.check(attn.attn_device_status(), "device status")
+        o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), scale, causal)
+        if with_lse:
+            assert_close(to64(o), o_ref, to64(lse), lse_ref, what=f"seed {seed}")
+        else:
+            assert lse is None
+            assert_close(to64(o), o_ref, what=f"seed {seed}")
+
+
+def test_host_forward_is_ordered_on_the_callers_stream(attn):
+    """Work enqueued on the stream after the call sees the copied-back output,
+    and the call waits for work enqueued before it."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N, d = 1, 4, 4, 512, 64
+    scale = scale_of(d)
+    q, k, v = prefill_inputs(8, B, Hq, Hkv, N, d, dev)
+    o_ref, _ = attn.forward(q, k, v, causal=False, scale=scale)
+    s = torch.cuda.Stream()
+    hq, hk, hv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
+    o_h = torch.zeros(q.shape, dtype=q.dtype, pin_memory=True)
+    back = torch.empty_like(q)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        # fill the host inputs from the device on the same stream, then run
+        for src, dst in ((q, hq), (k, hk), (v, hv)):
+            dst.copy_(src, non_blocking=True)
+        attn.forward_host(hq, hk, hv, scale=scale, with_lse=False, kv_heads_per_chunk=1, out=(o_h, None),
+                          stream=s, synchronize=False)
+        back.copy_(o_h, non_blocking=True)
+    s.synchronize()
+    attn.check(attn.attn_device_status(), "device status")
+    assert torch.equal(back.view(torch.int16), o_ref.view(torch.int16))
