@@ -40,10 +40,10 @@ DEC = dict(B=8, Hq=64, Hkv=8, S=32768, d=128)
 # digest; after any change to them the bench reports null until re-captured.
 MEASURED_TRAFFIC = {
     "fwd": {"files": ["fwd_sm103.cu", "sm103_ptx.cuh", "tile_order.cuh"],
-            "sha256": "9229ea21e4cd0e235680fd0abfec9ea90e2dcbfaa290c4c59582b72d6fa9c160",
+            "sha256": "344139d333fad7e9818e453d0773a4d7b1cdb18bf2e3ce5f4733b4cb888cce42",
             # MHA B=1 H=128 d=128, head-first, captured at N=32768 and N=8192 (one-pass
             # capture of dram__bytes_read.sum + dram__bytes_write.sum)
-            "bytes_by_n": {32768: 3232415488 + 1087872512, 8192: 806408960 + 251140864}},
+            "bytes_by_n": {32768: 3234135040 + 1089067776, 8192: 805678336 + 251972864}},
     "decode": {"files": ["decode_sm103.cu", "sm103_ptx.cuh"],
                "sha256": "84c5c7a81f5fab826c433a44b2424358cd61441d6fd4f7a86ee0e3df18b4451c",
                # GQA decode B=8 Hq=64 Hkv=8 d=128, 4 splits, captured at 8192 keys;
