@@ -51,6 +51,12 @@ SMALL = [
     (2, 2, 2, 300, 64, True),
     (1, 4, 4, 2048, 128, False),
     (1, 4, 2, 1537, 64, True),
+    # lengths around multiples of 192 keys
+    (1, 2, 2, 192, 64, True),
+    (1, 2, 2, 193, 64, False),
+    (1, 4, 2, 385, 64, True),
+    (2, 2, 1, 577, 56, True),
+    (1, 2, 2, 767, 64, False),
 ]
 
 
@@ -192,20 +198,22 @@ def test_full_size_sampled_rows(attn, name, B, Hq, Hkv, N, d, causal):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_scores_rising_far_above_the_first_block(attn, d, causal):
-    """Keys past the first 256 score about 64 (natural log units) above the
-    first ones, more than 2^60 in the exponent's base-2 range, so the
+@pytest.mark.parametrize("jump", [256, 150, 352])
+def test_scores_rising_far_above_the_first_block(attn, d, causal, jump):
+    """Keys from `jump` on score about 64 (natural log units) above the
+    earlier ones, more than 2^60 in the exponent's base-2 range, so the
     softmax's running reference maximum has to move mid-row (its
-    recomputation path); the result must still match the oracle."""
+    recomputation path); the result must still match the oracle.  The jump
+    lands at the start of a 128-key block (256) or inside one (150, 352)."""
     dev = torch.device("cuda")
     B, H, N = 1, 2, 700
     g = torch.Generator().manual_seed(5)
     q = torch.ones(B, H, N, d) + 0.01 * torch.randn(B, H, N, d, generator=g)
-    level = torch.where(torch.arange(N) < 256, 0.0, 8.0).view(1, 1, N, 1)
+    level = torch.where(torch.arange(N) < jump, 0.0, 8.0).view(1, 1, N, 1)
     k = level * torch.ones(B, H, N, d) + 0.05 * torch.randn(B, H, N, d, generator=g)
     v = torch.randn(B, H, N, d, generator=g)
     q, k, v = (t.to(torch.bfloat16).to(dev) for t in (q, k, v))
     scale = 1.0 / 8.0
     o, lse = _run(attn, q, k, v, causal, scale)
     o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), scale, causal)
-    assert_close(to64(o), o_ref, to64(lse), lse_ref, what=f"rising scores d={d} causal={causal}")
+    assert_close(to64(o), o_ref, to64(lse), lse_ref, what=f"rising scores d={d} causal={causal} jump={jump}")
