@@ -26,6 +26,17 @@
  *    CUDA call and leave all memory untouched.
  *  - Return value: ATTN_OK (0) or one of the negative ATTN_ERR_* codes.
  *    attn_strerror() gives a message for each.
+ *  - CUDA graphs: the launches of attn_fwd, attn_fwd_ex, attn_fwd_host,
+ *    attn_bwd and the decode entry points can be captured into a CUDA graph
+ *    on `stream` and replayed; a replay reads what the buffers hold at replay
+ *    time (the ragged decode's seqlens included: it plans on the device).
+ *    Make one ordinary call per device first (it sets up per-device state:
+ *    kernel attributes, scratch addresses, the die map, the host-copy
+ *    streams).  The persistent forward and backward kernels take one of 64
+ *    scheduler slots per launch and a captured launch keeps its slot, so
+ *    replay it where it cannot overlap 64 other forward or backward launches
+ *    (for example, on the stream that issues them).  attn_device_status
+ *    synchronises and is not captured.
  *  - Device-side bounded waits: every spin on a barrier inside the kernels
  *    is limited in time.  A wait that runs out sets a device status word and
  *    the kernel returns early (its outputs are then undefined).
