@@ -51,7 +51,7 @@ SIGNATURES = {
     "attn_decode_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "attn_decode_varlen_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "attn_decode_num_splits": (_I, [_I, _I, _I, _I]),
-    "attn_tile_map": (_I, [_I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
+    "attn_tile_map": (_I, [_I, _I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
     "attn_tile_map_die_split": (_I, [_I, _I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
     "attn_die_map": (_I, [_IP, _I, _FP]),
     "attn_fwd_units": (_LL, [_I, _I, _I]),
@@ -203,9 +203,9 @@ def attn_decode_num_splits(B, Hq, Hkv, max_seqlen) -> int:
     return int(lib().attn_decode_num_splits(B, Hq, Hkv, max_seqlen))
 
 
-def attn_tile_map(tile_order, B, Hq, N, causal, unit):
+def attn_tile_map(tile_order, B, Hq, Hkv, N, causal, unit):
     b, h, m = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    rc = lib().attn_tile_map(int(tile_order), B, Hq, N, int(bool(causal)), int(unit),
+    rc = lib().attn_tile_map(int(tile_order), B, Hq, Hkv, N, int(bool(causal)), int(unit),
                              ctypes.byref(b), ctypes.byref(h), ctypes.byref(m))
     check(rc, "attn_tile_map")
     return b.value, h.value, m.value

@@ -113,13 +113,13 @@ long long attn_fwd_units(int B, int Hq, int N) {
     return (long long)B * Hq * unit_blocks(N);
 }
 
-int attn_tile_map(int tile_order, int B, int Hq, int N, int causal, long long unit, int *b, int *h,
+int attn_tile_map(int tile_order, int B, int Hq, int Hkv, int N, int causal, long long unit, int *b, int *h,
                   int *m) {
-    if (!b || !h || !m || B <= 0 || Hq <= 0 || N <= 0) return ATTN_ERR_ARG;
+    if (!b || !h || !m || B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || Hq % Hkv) return ATTN_ERR_ARG;
     if (tile_order < kHeadFirst || tile_order > kNaiveHeadFirst) return ATTN_ERR_ARG;
     const long long total = attn_fwd_units(B, Hq, N);
     if (unit < 0 || unit >= total) return ATTN_ERR_ARG;
-    const Tile t = unit_to_tile(tile_order, unit, Hq, unit_blocks(N), causal ? 1 : 0);
+    const Tile t = unit_to_tile(tile_order, unit, Hq, Hq / Hkv, unit_blocks(N), causal ? 1 : 0);
     *b = t.b;
     *h = t.h;
     *m = t.m;
@@ -133,7 +133,7 @@ int attn_tile_map_die_split(int B, int Hq, int Hkv, int N, int causal, int die, 
     const int nb = unit_blocks(N);
     const long long u = die_split_unit(die, k, B, Hkv, Hq / Hkv, nb);
     if (u < 0) return ATTN_ERR_ARG;
-    const Tile t = unit_to_tile(kHeadFirst, u, Hq, nb, causal ? 1 : 0);
+    const Tile t = unit_to_tile(kHeadFirst, u, Hq, Hq / Hkv, nb, causal ? 1 : 0);
     *b = t.b;
     *h = t.h;
     *m = t.m;

@@ -111,7 +111,7 @@ struct UnitWork {
 };
 
 __device__ __forceinline__ UnitWork unit_work(const Params &p, long long u) {
-    const Tile t = unit_to_tile(p.order, u, p.Hq, p.nb, p.causal);
+    const Tile t = unit_to_tile(p.order, u, p.Hq, p.G, p.nb, p.causal);
     UnitWork w;
     w.b = t.b;
     w.h = t.h;

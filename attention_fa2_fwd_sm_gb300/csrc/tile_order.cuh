@@ -30,12 +30,16 @@ struct Tile {
 
 __host__ __device__ inline int unit_blocks(int N) { return (N + kUnitRows - 1) / kUnitRows; }
 
-// Linear unit id -> tile.  Head-first (and naive head-first): the block index
-// runs fastest, then the query head, then the batch entry; because query
-// heads of one KV group are contiguous, a group's units are consecutive.
+// Linear unit id -> tile (G = Hq / Hkv query heads per KV head).
+// Naive head-first: the block index runs fastest, then the query head, then
+// the batch entry.  Head-first (and die-split, whose unit ids are head-first
+// ids): the same ACC-major order -- query heads of one KV group are
+// contiguous, so an ACC's G * nb units are consecutive -- except that inside
+// a causal GQA ACC the units go longest first across the ACC's heads (block
+// rank, then head), so the last ACC's long units do not start last.
 // Block-first: the query head runs fastest.  Causal: blocks are visited in
 // descending order so the longest units start first.
-__host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int nb, int causal) {
+__host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int G, int nb, int causal) {
     Tile t;
     int r;
     if (order == kBlockFirst) {
@@ -43,6 +47,14 @@ __host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int
         long long bm = u / Hq;
         r = int(bm % nb);
         t.b = int(bm / nb);
+    } else if (order != kNaiveHeadFirst && causal && G > 1) {
+        const long long upa = (long long)G * nb;  // units per ACC
+        const long long a = u / upa;             // ACC = b * Hkv + KV head
+        const int w = int(u % upa);
+        const int Hkv = Hq / G;
+        r = w / G;
+        t.h = int(a % Hkv) * G + w % G;
+        t.b = int(a / Hkv);
     } else {
         r = int(u % nb);
         long long bh = u / nb;

@@ -68,8 +68,9 @@ enum attn_status {
  *  HEAD_FIRST: all row blocks of one Attention Compute Cluster (the query
  *    heads sharing one KV head) before the next one, so CTAs running at the
  *    same time read the same K/V and reuse it in L2 (detail page, section 2
- *    Q2 and section 3 "before/after" table).  Causal units of a head run
- *    last-block-first (longest first).
+ *    Q2 and section 3 "before/after" table).  Inside an ACC the row blocks
+ *    of one head follow each other; for causal GQA the ACC's units instead
+ *    run longest first across its heads (block descending, then head).
  *  BLOCK_FIRST: all heads of one row block before the next row block (the
  *    pages' "Naive Block-first" baseline).
  *  NAIVE_HEAD_FIRST: head-first linear order, but one CTA per unit with the
@@ -301,9 +302,9 @@ int attn_decode_num_splits(int B, int Hq, int Hkv, int max_seqlen);
 /* Host-side view of the forward scheduler: unit `unit` of the order maps to
  * (*b, *h, *m) where m is the index of a 256-row block.  Pure host code; the
  * same function runs inside the kernel.  Orders 0-2 only (the die-split order
- * has one sequence per die: attn_tile_map_die_split).  Returns ATTN_OK or
- * ATTN_ERR_ARG. */
-int attn_tile_map(int tile_order, int B, int Hq, int N, int causal, long long unit,
+ * has one sequence per die: attn_tile_map_die_split).  Hkv matters for the
+ * causal head-first order only.  Returns ATTN_OK or ATTN_ERR_ARG. */
+int attn_tile_map(int tile_order, int B, int Hq, int Hkv, int N, int causal, long long unit,
                   int *b, int *h, int *m);
 
 /* The k-th unit (k >= 0) that die `die` (0 or 1) takes from its own ACCs

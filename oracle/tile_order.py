@@ -13,7 +13,9 @@ Exploiting GPU Architectural NUMA Effects", section 2 Q2 and section 3
 * head-first: all row blocks of one Attention Compute Cluster (the query
   heads that share one KV head) before the next one.  With contiguous GQA
   groups, (batch, kv group, head in group, block) order is simply
-  (batch, head, block).
+  (batch, head, block).  For causal attention with several query heads per
+  KV head the ACC's units go (block rank, head in group): every head's
+  longest unit, then every head's second longest, and so on.
 * block-first: all heads of one row block before the next row block.
 * naive head-first: the head-first linear order, but each unit is its own
   CTA and the hardware decides where it runs.
@@ -24,7 +26,7 @@ Exploiting GPU Architectural NUMA Effects", section 2 Q2 and section 3
 
 For causal attention the blocks of a head are visited last-block-first, so
 the longest units start first (the pages give only "ACC before next ACC";
-this within-ACC order is a reading).
+the within-ACC orders are readings).
 """
 from __future__ import annotations
 
@@ -38,12 +40,17 @@ def num_blocks(n: int, bm: int) -> int:
     return -(-n // bm)
 
 
-def unit_to_tile(order: int, u: int, batch: int, heads: int, nb: int, causal: bool):
-    """Linear unit id -> (b, h, m)."""
+def unit_to_tile(order: int, u: int, batch: int, heads: int, nb: int, causal: bool, group: int = 1):
+    """Linear unit id -> (b, h, m); ``group`` query heads share one KV head."""
     total = batch * heads * nb
     if not 0 <= u < total:
         raise ValueError("unit out of range")
-    if order in (HEAD_FIRST, NAIVE_HEAD_FIRST):
+    if order == HEAD_FIRST and causal and group > 1:
+        acc, w = divmod(u, group * nb)       # ACC = (batch entry, KV head)
+        r, head_in_group = divmod(w, group)  # block rank, then head
+        b, kv_head = divmod(acc, heads // group)
+        h = kv_head * group + head_in_group
+    elif order in (HEAD_FIRST, NAIVE_HEAD_FIRST):
         bh, r = divmod(u, nb)
         b, h = divmod(bh, heads)
     elif order == BLOCK_FIRST:
@@ -88,14 +95,22 @@ def die_split_sequence(die: int, batch: int, hq: int, hkv: int, nb: int, causal:
     takes them.  The ACCs (batch entry b, KV head g; ACC index a = b*hkv + g)
     are dealt round-robin, ACC a to die a % dies, and each die visits its ACCs
     in increasing a, each ACC in head-first order: the ACC's query heads one
-    after the other, every row block of a head before the next head."""
+    after the other, every row block of a head before the next head -- or,
+    causal with several query heads per KV head, block rank by block rank
+    (longest first), the ACC's heads inside each rank."""
     g_size = hq // hkv
     out = []
     for a in range(batch * hkv):
         if a % dies != die:
             continue
         b, kvh = divmod(a, hkv)
-        for h in range(kvh * g_size, (kvh + 1) * g_size):
+        heads = range(kvh * g_size, (kvh + 1) * g_size)
+        if causal and g_size > 1:
             for r in range(nb):
-                out.append((b, h, nb - 1 - r if causal else r))
+                for h in heads:
+                    out.append((b, h, nb - 1 - r))
+        else:
+            for h in heads:
+                for r in range(nb):
+                    out.append((b, h, nb - 1 - r if causal else r))
     return out

@@ -50,19 +50,23 @@ def test_missing_library_fails_loudly(monkeypatch):
 
 @pytest.mark.parametrize("order", T.ORDERS)
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("B,H,N", [(1, 2, 256), (2, 3, 300), (1, 8, 4096), (3, 5, 1)])
-def test_scheduler_matches_the_definitions(L, order, causal, B, H, N):
+@pytest.mark.parametrize("B,H,Hkv,N", [(1, 2, 2, 256), (2, 3, 3, 300), (1, 8, 8, 4096), (3, 5, 5, 1),
+                                       (1, 8, 2, 1300), (2, 6, 3, 600), (1, 64, 8, 2048)])
+def test_scheduler_matches_the_definitions(L, order, causal, B, H, Hkv, N):
     nb = T.num_blocks(N, 256)
     assert attn.attn_fwd_units(B, H, N) == B * H * nb
     for u in range(B * H * nb):
-        assert attn.attn_tile_map(order, B, H, N, causal, u) == T.unit_to_tile(order, u, B, H, nb, causal)
+        assert (attn.attn_tile_map(order, B, H, Hkv, N, causal, u)
+                == T.unit_to_tile(order, u, B, H, nb, causal, H // Hkv))
 
 
 def test_scheduler_rejects_bad_units(L):
     with pytest.raises(attn.AttnError):
-        attn.attn_tile_map(0, 1, 2, 256, False, 2)
+        attn.attn_tile_map(0, 1, 2, 2, 256, False, 2)
     with pytest.raises(attn.AttnError):
-        attn.attn_tile_map(7, 1, 2, 256, False, 0)
+        attn.attn_tile_map(7, 1, 2, 2, 256, False, 0)
+    with pytest.raises(attn.AttnError):
+        attn.attn_tile_map(0, 1, 6, 4, 256, True, 0)  # Hq % Hkv != 0
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -78,7 +82,7 @@ def test_die_split_scheduler_matches_the_definition(L, causal, B, Hq, Hkv, N):
 
 def test_tile_map_rejects_the_die_split_order(L):
     with pytest.raises(attn.AttnError):
-        attn.attn_tile_map(3, 1, 2, 256, False, 0)
+        attn.attn_tile_map(3, 1, 2, 2, 256, False, 0)
     assert attn.attn_tile_map_die_split(1, 2, 2, 256, False, 2, 0) is None  # no die 2
     assert attn.attn_tile_map_die_split(1, 2, 2, 256, False, 0, -1) is None
 

@@ -6,10 +6,27 @@ from oracle import tile_order as T
 
 @pytest.mark.parametrize("order", T.ORDERS)
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("B,H,nb", [(1, 2, 1), (1, 8, 5), (2, 3, 4), (4, 128, 3), (1, 64, 32)])
-def test_orders_are_bijections(order, causal, B, H, nb):
-    seen = {T.unit_to_tile(order, u, B, H, nb, causal) for u in range(B * H * nb)}
+@pytest.mark.parametrize("B,H,nb,G", [(1, 2, 1, 1), (1, 8, 5, 1), (2, 3, 4, 1), (4, 128, 3, 1), (1, 64, 32, 1),
+                                      (1, 8, 5, 4), (2, 6, 4, 3), (1, 64, 32, 8), (3, 2, 1, 2)])
+def test_orders_are_bijections(order, causal, B, H, nb, G):
+    seen = {T.unit_to_tile(order, u, B, H, nb, causal, G) for u in range(B * H * nb)}
     assert seen == {(b, h, m) for b in range(B) for h in range(H) for m in range(nb)}
+
+
+@pytest.mark.parametrize("B,Hq,G,nb", [(1, 16, 4, 5), (2, 6, 3, 4), (1, 64, 8, 32)])
+def test_causal_gqa_head_first_runs_each_acc_longest_first(B, Hq, G, nb):
+    """Each ACC's G * nb units are consecutive, and inside the ACC the units
+    come in non-increasing causal length (block index descending), every
+    head of the group at each length."""
+    seq = [T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, True, G) for u in range(B * Hq * nb)]
+    upa = G * nb
+    for a in range(B * Hq // G):
+        acc = seq[a * upa:(a + 1) * upa]
+        assert {(b, h // G) for b, h, _ in acc} == {divmod(a, Hq // G)}
+        ms = [m for _, _, m in acc]
+        assert ms == sorted(ms, reverse=True)
+        for i in range(0, upa, G):
+            assert sorted(h % G for _, h, _ in acc[i:i + G]) == list(range(G))
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -38,9 +55,15 @@ def test_block_first_cycles_heads_innermost():
 
 
 def test_naive_head_first_has_the_head_first_linear_order():
+    """Equal except for causal GQA, where naive head-first keeps the linear
+    (head, block) order of a one-CTA-per-unit launch."""
     for u in range(2 * 3 * 4):
         assert (T.unit_to_tile(T.NAIVE_HEAD_FIRST, u, 2, 3, 4, True)
                 == T.unit_to_tile(T.HEAD_FIRST, u, 2, 3, 4, True))
+        assert (T.unit_to_tile(T.NAIVE_HEAD_FIRST, u, 2, 6, 4, False, 2)
+                == T.unit_to_tile(T.HEAD_FIRST, u, 2, 6, 4, False, 2))
+    assert ([T.unit_to_tile(T.NAIVE_HEAD_FIRST, u, 1, 4, 3, True, 2) for u in range(4)]
+            == [(0, 0, 2), (0, 0, 1), (0, 0, 0), (0, 1, 2)])
 
 
 @pytest.mark.parametrize("B", [1, 2, 4])
@@ -117,13 +140,14 @@ def test_die_split_each_die_is_head_first_over_its_accs():
     """Per die the order is the head-first order restricted to that die's
     ACCs; for one ACC per die it is exactly the head-first order of that ACC."""
     B, Hq, Hkv, nb = 1, 4, 2, 3
-    hf = [T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, True) for u in range(B * Hq * nb)]
     G = Hq // Hkv
+    hf = [T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, True, G) for u in range(B * Hq * nb)]
     for d in (0, 1):
         assert T.die_split_sequence(d, B, Hq, Hkv, nb, True) == [x for x in hf if x[1] // G == d]
 
 
-def test_die_split_with_one_die_is_head_first():
+@pytest.mark.parametrize("causal", [False, True])
+def test_die_split_with_one_die_is_head_first(causal):
     B, Hq, Hkv, nb = 2, 6, 3, 4
-    assert T.die_split_sequence(0, B, Hq, Hkv, nb, False, dies=1) == [
-        T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, False) for u in range(B * Hq * nb)]
+    assert T.die_split_sequence(0, B, Hq, Hkv, nb, causal, dies=1) == [
+        T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, causal, Hq // Hkv) for u in range(B * Hq * nb)]
