@@ -673,6 +673,15 @@ __device__ __forceinline__ QUnit2 q_unit2(const Params &p, long long u) {
         const long long bm = u / p.Hq;
         r = int(bm % nq);
         w.b = int(bm / nq);
+    } else if (p.order == kHeadFirst && p.causal && p.G > 1) {
+        // as the forward's head-first order: a causal GQA ACC's units run
+        // longest first across its query heads (block rank, then head)
+        const long long upa = (long long)p.G * nq;
+        const long long a = u / upa;  // ACC = b * Hkv + KV head
+        const int wi = int(u % upa);
+        r = wi / p.G;
+        w.h = int(a % p.Hkv) * p.G + wi % p.G;
+        w.b = int(a / p.Hkv);
     } else {
         r = int(u % nq);
         const long long bh = u / nq;
