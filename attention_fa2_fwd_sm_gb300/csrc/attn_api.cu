@@ -43,12 +43,12 @@ EncodeTiledFn encode_fn() {
 int current_num_sms() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-    static int cached[64] = {0};
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    static int cached[kMaxDevices] = {0};
+    if (dev >= 0 && dev < kMaxDevices && cached[dev] > 0) return cached[dev];
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         return -1;
-    if (dev >= 0 && dev < 64) cached[dev] = n;
+    if (dev >= 0 && dev < kMaxDevices) cached[dev] = n;
     return n;
 }
 

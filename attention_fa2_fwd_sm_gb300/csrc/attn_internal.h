@@ -69,6 +69,17 @@ HostChunkLayout host_chunk_layout(int Hq, int Hkv, int N, int d, int kv_heads_pe
 int host_default_chunk(int Hq, int Hkv, int N);
 int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream);
 
+// Kernel attributes (the dynamic shared-memory limit) belong to the current
+// device, so the launchers set them once per device: slot_for_device()
+// gives the current device's index into a per-device flag array, or -1 when
+// it is out of range (then the attributes are set on every launch).
+constexpr int kMaxDevices = 64;
+inline int slot_for_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
 // Record a failed CUDA call for attn_last_error() (this thread) and return
 // ATTN_ERR_CUDA.
 int note_cuda_error(cudaError_t e, const char *where);

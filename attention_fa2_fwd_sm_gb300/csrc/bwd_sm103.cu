@@ -1071,8 +1071,9 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
         !encode_bf16_3d(&mv, a.v, dd, uint64_t(a.N), uint64_t(a.B) * a.Hkv, 64, kRows))
         return note_cuda_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled (backward)");
 
-    static bool attr_set = false;  // per instantiation
-    if (!attr_set) {
+    static bool attr_set[kMaxDevices] = {};  // per instantiation and device
+    const int dev = slot_for_device();
+    if (dev < 0 || !attr_set[dev]) {
         // The setmaxnreg split assumes the launch register count; refuse a
         // build that differs (its setmaxnreg.inc could never complete).
         cudaFuncAttributes fa, fb;
@@ -1087,7 +1088,7 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CB::kSmemBytes);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(backward kernels)");
-        attr_set = true;
+        if (dev >= 0) attr_set[dev] = true;
     }
     static std::atomic<unsigned int> launch_seq{0};
 

@@ -514,12 +514,13 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
     p.num_splits = a.num_splits;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_ns = a.wait_ns;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static bool attr_set[kMaxDevices] = {};  // per instantiation and device
+    const int dev = slot_for_device();
+    if (dev < 0 || !attr_set[dev]) {
         const cudaError_t e = cudaFuncSetAttribute(
             decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(decode_kernel)");
-        attr_set = true;
+        if (dev >= 0) attr_set[dev] = true;
     }
     if (a.plan) {
         varlen_plan_kernel<<<1, 256, 0, stream>>>(a.seqlens, a.B, a.max_seqlen, a.Hkv, a.varlen_target,
@@ -553,7 +554,6 @@ int decode_launch(const DecodeLaunch &a, cudaStream_t stream) {
 
 cudaError_t decode_noalloc_scratch(void **ptr) {
     // One lookup per device, made with that device current; later calls reuse it.
-    constexpr int kMaxDevices = 64;
     static void *addr[kMaxDevices] = {nullptr};
     static std::mutex mu;
     int dev = 0;

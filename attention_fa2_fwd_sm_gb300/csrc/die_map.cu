@@ -89,7 +89,7 @@ struct DieState {
 };
 
 std::mutex g_die_mutex;
-DieState g_die_state[64];
+DieState g_die_state[kMaxDevices];
 
 void halves(DieState &st) {
     st.die.assign(st.n, 0);
@@ -240,7 +240,7 @@ int ensure(DieState **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return note_cuda_error(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return note_cuda_error(cudaErrorInvalidDevice, "device index (die map)");
+    if (dev < 0 || dev >= kMaxDevices) return note_cuda_error(cudaErrorInvalidDevice, "device index (die map)");
     std::lock_guard<std::mutex> lock(g_die_mutex);
     DieState &st = g_die_state[dev];
     if (!st.done) {

@@ -27,7 +27,6 @@ namespace attn {
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 constexpr int kSlots = 2;
 
 struct HostPipe {

@@ -655,8 +655,9 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
         const int rc = die_map_device(&p.die_of_sm);
         if (rc < 0) return rc;
     }
-    static bool attr_set = false;  // per instantiation; the attribute is per function
-    if (!attr_set) {
+    static bool attr_set[kMaxDevices] = {};  // per instantiation and device
+    const int dev = slot_for_device();
+    if (dev < 0 || !attr_set[dev]) {
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, fwd_kernel<D>);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncGetAttributes(fwd_kernel)");
@@ -668,7 +669,7 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
         e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(fwd_kernel)");
-        attr_set = true;
+        if (dev >= 0) attr_set[dev] = true;
     }
     long long grid = p.total_units;
     if (a.order != kNaiveHeadFirst && grid > a.num_sms) grid = a.num_sms;
