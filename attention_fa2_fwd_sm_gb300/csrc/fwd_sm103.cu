@@ -110,8 +110,13 @@ struct UnitWork {
     int nmax;
 };
 
+// kGrouped: the launch maps units with unit_to_tile_grouped_causal (causal
+// GQA in a head-first order); it is a template parameter so that the other
+// launches compile without that code.
+template <bool kGrouped>
 __device__ __forceinline__ UnitWork unit_work(const Params &p, long long u) {
-    const Tile t = unit_to_tile(p.order, u, p.Hq, p.G, p.nb, p.causal);
+    const Tile t = kGrouped ? unit_to_tile_grouped_causal(u, p.Hq, p.G, p.nb)
+                            : unit_to_tile(p.order, u, p.Hq, p.nb, p.causal);
     UnitWork w;
     w.b = t.b;
     w.h = t.h;
@@ -161,7 +166,7 @@ __device__ __forceinline__ int last_user(const UnitWork &w, int j) {
     return last;
 }
 
-template <int D>
+template <int D, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -245,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 unit_q[qs] = int(u);
                 mbar_arrive(bar(C::kBarUQFull + qs));
                 if (u < 0) break;
-                const UnitWork w = unit_work(p, u);
+                const UnitWork w = unit_work<kGrouped>(p, u);
                 for (int t = 0; t < kNT && ok; ++t) {
                     if (w.nkv[t] == 0) continue;
                     if (q_loads[t] > 0)
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const long long u = unit_q[qs];
                 mbar_arrive(bar(C::kBarUQEmpty + qs));
                 if (u < 0) break;
-                const UnitWork w = unit_work(p, u);
+                const UnitWork w = unit_work<kGrouped>(p, u);
                 const long long f0 = fills;  // K_j at f0 + 2j, V_j at f0 + 2j + 1
                 // prologue: S(t, 0) = Q(t) K_0^T
                 ok = wait_slot(f0);
@@ -460,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarUQEmpty + qs));
             if (u < 0) break;
-            const UnitWork w = unit_work(p, u);
+            const UnitWork w = unit_work<kGrouped>(p, u);
             const long long f0 = kv_base;  // K_j at ring position f0 + 2j
             kv_base += 2 * (long long)w.nmax;
             const int nkv = w.nkv[t];
@@ -655,26 +660,27 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
         const int rc = die_map_device(&p.die_of_sm);
         if (rc < 0) return rc;
     }
-    static bool attr_set[kMaxDevices] = {};  // per instantiation and device
+    const bool grouped = grouped_causal_order(a.order, p.G, p.causal);
+    auto kernel = grouped ? fwd_kernel<D, true> : fwd_kernel<D, false>;
+    static bool attr_set[2][kMaxDevices] = {};  // per instantiation and device
     const int dev = slot_for_device();
-    if (dev < 0 || !attr_set[dev]) {
+    if (dev < 0 || !attr_set[grouped][dev]) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, fwd_kernel<D>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncGetAttributes(fwd_kernel)");
         // The setmaxnreg split assumes the launch register count; refuse to
         // launch a build that differs (its setmaxnreg.inc could never finish).
         if (fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
             return note_cuda_error(cudaErrorInvalidConfiguration,
                                    "fwd_kernel register count differs from the setmaxnreg split");
-        e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(fwd_kernel)");
-        if (dev >= 0) attr_set[dev] = true;
+        if (dev >= 0) attr_set[grouped][dev] = true;
     }
     long long grid = p.total_units;
     if (a.order != kNaiveHeadFirst && grid > a.num_sms) grid = a.num_sms;
     if (grid > 0x7fffffffLL) return -2;
-    fwd_kernel<D><<<dim3(unsigned(grid)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, p);
+    kernel<<<dim3(unsigned(grid)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? 0 : note_cuda_error(e, "fwd_kernel launch");
 }

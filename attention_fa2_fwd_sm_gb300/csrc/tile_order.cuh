@@ -30,16 +30,12 @@ struct Tile {
 
 __host__ __device__ inline int unit_blocks(int N) { return (N + kUnitRows - 1) / kUnitRows; }
 
-// Linear unit id -> tile (G = Hq / Hkv query heads per KV head).
-// Naive head-first: the block index runs fastest, then the query head, then
-// the batch entry.  Head-first (and die-split, whose unit ids are head-first
-// ids): the same ACC-major order -- query heads of one KV group are
-// contiguous, so an ACC's G * nb units are consecutive -- except that inside
-// a causal GQA ACC the units go longest first across the ACC's heads (block
-// rank, then head), so the last ACC's long units do not start last.
+// Linear unit id -> tile.  Head-first (and naive head-first): the block index
+// runs fastest, then the query head, then the batch entry; because query
+// heads of one KV group are contiguous, a group's units are consecutive.
 // Block-first: the query head runs fastest.  Causal: blocks are visited in
 // descending order so the longest units start first.
-__host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int G, int nb, int causal) {
+__host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int nb, int causal) {
     Tile t;
     int r;
     if (order == kBlockFirst) {
@@ -47,14 +43,6 @@ __host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int
         long long bm = u / Hq;
         r = int(bm % nb);
         t.b = int(bm / nb);
-    } else if (order != kNaiveHeadFirst && causal && G > 1) {
-        const long long upa = (long long)G * nb;  // units per ACC
-        const long long a = u / upa;             // ACC = b * Hkv + KV head
-        const int w = int(u % upa);
-        const int Hkv = Hq / G;
-        r = w / G;
-        t.h = int(a % Hkv) * G + w % G;
-        t.b = int(a / Hkv);
     } else {
         r = int(u % nb);
         long long bh = u / nb;
@@ -63,6 +51,34 @@ __host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int
     }
     t.m = causal ? (nb - 1 - r) : r;
     return t;
+}
+
+// Head-first (and die-split, whose unit ids are head-first ids) for causal
+// attention with G > 1 query heads per KV head: still ACC-major (an ACC's
+// G * nb units are consecutive), but inside the ACC the units go longest
+// first across its query heads -- block rank, then head -- so that the last
+// ACC's long units do not start last.
+__host__ __device__ inline Tile unit_to_tile_grouped_causal(long long u, int Hq, int G, int nb) {
+    const long long upa = (long long)G * nb;  // units per ACC
+    const long long a = u / upa;             // ACC = b * Hkv + KV head
+    const int w = int(u % upa);
+    const int Hkv = Hq / G;
+    Tile t;
+    t.h = int(a % Hkv) * G + w % G;
+    t.b = int(a / Hkv);
+    t.m = nb - 1 - w / G;
+    return t;
+}
+
+// Whether an order uses the grouped causal mapping above.
+__host__ __device__ inline bool grouped_causal_order(int order, int G, int causal) {
+    return causal && G > 1 && (order == kHeadFirst || order == kDieSplitHeadFirst);
+}
+
+// The mapping of any order (host view and tests).
+__host__ __device__ inline Tile unit_to_tile(int order, long long u, int Hq, int G, int nb, int causal) {
+    return grouped_causal_order(order, G, causal) ? unit_to_tile_grouped_causal(u, Hq, G, nb)
+                                                  : unit_to_tile(order, u, Hq, nb, causal);
 }
 
 // Die-split head-first: the Attention Compute Clusters (ACC: the query heads
