@@ -142,6 +142,9 @@ __global__ void __launch_bounds__(kThreads)
     const int g = p.plan ? blockIdx.x : blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // In work-list mode the plan kernel ahead of this grid may still be
+    // running (programmatic launch): wait for its list.
+    griddep_wait();
     int b, lo, hi;
     if (p.plan) {
         // Varlen: this CTA is work item `split` of the plan (the grid is an
@@ -306,6 +309,7 @@ __global__ void __launch_bounds__(kThreads)
     }
 
     // ------------------------------------------------ combine the four warps
+    griddep_launch_dependents();  // the merge grid may be scheduled now
     __syncthreads();
     if (*abort_flag) {
         // A wait ran out somewhere.  Before the CTA exits, wait (bounded, with
@@ -385,6 +389,7 @@ __global__ void __launch_bounds__(kThreads)
 template <int D>
 __global__ void __launch_bounds__(D) merge_kernel(const float *ws_o, const float *ws_lse,
                                                   __nv_bfloat16 *o, int num_splits) {
+    griddep_wait();  // launched behind the decode grid, which writes the partials
     const int bh = blockIdx.x, col = threadIdx.x;
     const float *lse = ws_lse + (size_t)bh * num_splits;
     const float *po = ws_o + (size_t)bh * num_splits * D;
@@ -409,6 +414,7 @@ __global__ void __launch_bounds__(256) varlen_plan_kernel(const int *seqlens, in
                                                           long long target, int min_chunk, int *plan) {
     __shared__ long long warp_part[8];
     __shared__ int chunk_s;
+    griddep_launch_dependents();  // the decode grid may be scheduled; it waits for this one
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     const int per = (B + 255) / 256;  // consecutive sequences per thread
     const int b0 = min(t * per, B), b1 = min(b0 + per, B);
@@ -474,6 +480,7 @@ __global__ void __launch_bounds__(256) varlen_plan_kernel(const int *seqlens, in
 template <int D>
 __global__ void __launch_bounds__(D) merge_varlen_kernel(const int *plan, int B, int Hq, const float *ws_o,
                                                          const float *ws_lse, __nv_bfloat16 *o) {
+    griddep_wait();  // launched behind the decode grid, which writes the partials
     const int bh = blockIdx.x, col = threadIdx.x;
     const int b = bh / Hq, h = bh % Hq;
     const int f = plan[2 + b], n = plan[2 + B + b];
@@ -488,6 +495,25 @@ __global__ void __launch_bounds__(D) merge_varlen_kernel(const int *plan, int B,
         }
     }
     o[(size_t)bh * D + col] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
+}
+
+// Launch `kernel` allowing it to start before the grid ahead of it on the
+// stream has finished (it must griddep_wait() before reading that grid's
+// output).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <int D>
@@ -522,24 +548,27 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(decode_kernel)");
         if (dev >= 0) attr_set[dev] = true;
     }
+    // The kernels after the first are launched with programmatic stream
+    // serialization: each may be scheduled while the one ahead drains and
+    // waits (griddep_wait) for it before touching its output.
     if (a.plan) {
         varlen_plan_kernel<<<1, 256, 0, stream>>>(a.seqlens, a.B, a.max_seqlen, a.Hkv, a.varlen_target,
                                                   a.varlen_min_chunk, a.plan);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return note_cuda_error(e, "varlen_plan_kernel launch");
-        decode_kernel<D><<<dim3(a.Hkv, a.varlen_max_items, 1), dim3(kThreads), C::kSmemBytes, stream>>>(mk, mv, p);
-        e = cudaGetLastError();
+        e = launch_programmatic(decode_kernel<D>, dim3(a.Hkv, a.varlen_max_items, 1), dim3(kThreads),
+                                C::kSmemBytes, stream, mk, mv, p);
         if (e != cudaSuccess) return note_cuda_error(e, "decode_kernel launch (varlen)");
-        merge_varlen_kernel<D><<<dim3(a.B * a.Hq), dim3(D), 0, stream>>>(a.plan, a.B, a.Hq, a.ws_o, a.ws_lse, p.o);
-        e = cudaGetLastError();
+        e = launch_programmatic(merge_varlen_kernel<D>, dim3(a.B * a.Hq), dim3(D), 0, stream,
+                                (const int *)a.plan, a.B, a.Hq, (const float *)a.ws_o, (const float *)a.ws_lse, p.o);
         return e == cudaSuccess ? 0 : note_cuda_error(e, "merge_varlen_kernel launch");
     }
     decode_kernel<D><<<dim3(a.num_splits, a.Hkv, a.B), dim3(kThreads), C::kSmemBytes, stream>>>(mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return note_cuda_error(e, "decode_kernel launch");
     if (a.num_splits > 1) {
-        merge_kernel<D><<<dim3(a.B * a.Hq), dim3(D), 0, stream>>>(a.ws_o, a.ws_lse, p.o, a.num_splits);
-        e = cudaGetLastError();
+        e = launch_programmatic(merge_kernel<D>, dim3(a.B * a.Hq), dim3(D), 0, stream, (const float *)a.ws_o,
+                                (const float *)a.ws_lse, p.o, a.num_splits);
         if (e != cudaSuccess) return note_cuda_error(e, "merge_kernel launch");
     }
     return 0;

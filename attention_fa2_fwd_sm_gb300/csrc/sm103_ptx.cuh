@@ -139,6 +139,18 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, ui
     }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A grid launched with programmatic stream serialization may start before
+// the grid ahead of it on the stream has finished.  griddep_wait() blocks
+// until that grid has completed and its memory writes are visible (it
+// returns at once when the launch has no such dependency);
+// griddep_launch_dependents() lets the grid behind this one be scheduled
+// before this one completes.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
