@@ -40,15 +40,15 @@ DEC = dict(B=8, Hq=64, Hkv=8, S=32768, d=128)
 # digest; after any change to them the bench reports null until re-captured.
 MEASURED_TRAFFIC = {
     "fwd": {"files": ["fwd_sm103.cu", "sm103_ptx.cuh", "tile_order.cuh"],
-            "sha256": "344139d333fad7e9818e453d0773a4d7b1cdb18bf2e3ce5f4733b4cb888cce42",
+            "sha256": "6225aea524f735f54e261ef0cd1156a8743e1582d01f5180446998bb68dc6b5a",
             # MHA B=1 H=128 d=128, head-first, captured at N=32768 and N=8192 (one-pass
             # capture of dram__bytes_read.sum + dram__bytes_write.sum)
-            "bytes_by_n": {32768: 3234135040 + 1089067776, 8192: 805678336 + 251972864}},
+            "bytes_by_n": {32768: 3233736960 + 1090045184, 8192: 805450496 + 251987968}},
     "decode": {"files": ["decode_sm103.cu", "sm103_ptx.cuh"],
-               "sha256": "84c5c7a81f5fab826c433a44b2424358cd61441d6fd4f7a86ee0e3df18b4451c",
+               "sha256": "36aafa55e29c4da67d0c4eaa0986fdf0cc5872b11bfdd3c4927189e3ebe70d5f",
                # GQA decode B=8 Hq=64 Hkv=8 d=128, 4 splits, captured at 8192 keys;
                # the bytes scale with the keys streamed
-               "bytes_per_key": (268594176 + 3175424) / 8192.0, "batch": 8},
+               "bytes_per_key": (268593920 + 3189248) / 8192.0, "batch": 8},
 }
 
 
