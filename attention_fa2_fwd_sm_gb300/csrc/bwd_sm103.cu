@@ -643,7 +643,14 @@ struct QCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kChunkBytes = kRows * 128;
     static constexpr int kTileBytes = kRows * D * 2;
-    static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring of single tiles (K_j, V_j, K_j+1, ...)
+    // K/V ring of single tiles.  K tiles and V tiles have rings of their own:
+    // V_j is free once both dP products of block j are done, early in the
+    // block, while K_j is read by the block's last dQ product; sharing one
+    // round-robin ring put V_j+1 into K_j's slot and the MMA thread waited for
+    // it at the start of every block.
+    static constexpr int kKSlots = (D == 128) ? 2 : 4;
+    static constexpr int kVSlots = (D == 128) ? 1 : 2;
+    static constexpr int kStages = kKSlots + kVSlots;
     // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2]
     //           dp_full[2] ds_full[2] acc_full[2] acc_empty[2] uq_full[2] uq_empty[2] drain
     static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKVFull = 4, kBarKVEmpty = 4 + kStages,
@@ -656,6 +663,22 @@ struct QCfg {
     static constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 32 + 1024;
     static constexpr int kColDQ = 256;
 };
+
+// Fill f of the dQ pass's K/V stream: K_j at f = 2 j, V_j at f = 2 j + 1 (j
+// counts blocks over the CTA's units); its ring slot and how many earlier
+// fills used that slot (the mbarrier phase count).
+template <int D>
+__device__ __forceinline__ int dq_slot(long long f) {
+    using C = QCfg<D>;
+    const long long j = f >> 1;
+    return (f & 1) ? C::kKSlots + int(j % C::kVSlots) : int(j % C::kKSlots);
+}
+template <int D>
+__device__ __forceinline__ long long dq_use(long long f) {
+    using C = QCfg<D>;
+    const long long j = f >> 1;
+    return (f & 1) ? j / C::kVSlots : j / C::kKSlots;
+}
 
 // dq unit -> (b, h, m): m is a 256-row block; tile t covers rows m 256 + 128 t.
 struct QUnit2 {
@@ -770,9 +793,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long fills = 0;
             int q_loads[2] = {0, 0};
             bool ok = true;
+            long long last_use[C::kStages];  // use count of each slot's latest fill (-1: none)
+            for (int s = 0; s < C::kStages; ++s) last_use[s] = -1;
             auto emit = [&](const CUtensorMap *map, int blk, int plane) {
-                const int slot = int(fills % C::kStages);
-                const long long round = fills / C::kStages;
+                const int slot = dq_slot<D>(fills);
+                const long long round = dq_use<D>(fills);
                 if (round > 0 && !mbar_wait_bounded(bar(C::kBarKVEmpty + slot), uint32_t((round - 1) & 1),
                                                     p.wait_ns, abort_flag, status))
                     return false;
@@ -781,6 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(smem_u32(sKV + slot * C::kTileBytes + c * C::kChunkBytes), map, fb, c * 64,
                                 blk * kRows, plane);
+                last_use[slot] = round;
                 ++fills;
                 return true;
             };
@@ -823,10 +849,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const unsigned long long drain_ns = 1000000000ull;
                 volatile int no_abort = 0;
                 for (int s = 0; s < C::kStages; ++s) {
-                    if (fills <= s) continue;
-                    const long long last = fills - 1 - ((fills - 1 - s) % C::kStages);
-                    if (!mbar_wait_bounded(bar(C::kBarKVFull + s), uint32_t((last / C::kStages) & 1), drain_ns,
-                                           &no_abort, status))
+                    if (last_use[s] < 0) continue;
+                    if (!mbar_wait_bounded(bar(C::kBarKVFull + s), uint32_t(last_use[s] & 1), drain_ns, &no_abort,
+                                           status))
                         atomicOr(status, kStatusDrainTimeout);
                 }
                 for (int t = 0; t < 2; ++t)
@@ -843,9 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long fills = 0;
             int q_used[2] = {0, 0}, p_waits[2] = {0, 0}, ds_waits[2] = {0, 0}, units_done[2] = {0, 0};
             bool ok = true;
-            auto slot_of = [&](long long f) { return int(f % C::kStages); };
+            auto slot_of = [&](long long f) { return dq_slot<D>(f); };
             auto wait_fill = [&](long long f) {
-                return mbar_wait_bounded(bar(C::kBarKVFull + slot_of(f)), uint32_t((f / C::kStages) & 1), p.wait_ns,
+                return mbar_wait_bounded(bar(C::kBarKVFull + slot_of(f)), uint32_t(dq_use<D>(f) & 1), p.wait_ns,
                                          abort_flag, status);
             };
             auto kmaj = [&](long long f) { return smem_desc_sw128(smem_u32(sKV + slot_of(f) * C::kTileBytes), 16, 1024); };
