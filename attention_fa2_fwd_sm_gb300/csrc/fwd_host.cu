@@ -105,10 +105,20 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
     uint8_t *ho = static_cast<uint8_t *>(a.o_host);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
 
-#define ATTN_CK(call, what)                                          \
-    do {                                                             \
-        const cudaError_t ck_ = (call);                              \
-        if (ck_ != cudaSuccess) return note_cuda_error(ck_, what);   \
+    // On any failure after work was enqueued, the caller's stream still waits
+    // for whatever the internal streams hold (best effort), so buffers the
+    // caller releases after an error are not in use by a pending copy.
+    auto join_internal = [&]() {
+        for (cudaStream_t s : {hp.in, hp.comp, hp.out})
+            if (cudaEventRecord(hp.end, s) == cudaSuccess) cudaStreamWaitEvent(stream, hp.end, 0);
+    };
+#define ATTN_CK(call, what)                                   \
+    do {                                                      \
+        const cudaError_t ck_ = (call);                       \
+        if (ck_ != cudaSuccess) {                             \
+            join_internal();                                  \
+            return note_cuda_error(ck_, what);                \
+        }                                                     \
     } while (0)
 
     ATTN_CK(cudaEventRecord(hp.start, stream), "cudaEventRecord (host forward)");
@@ -145,7 +155,10 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
         f.Hq = hn;
         f.Hkv = gn;
         const int rc = fwd_launch(f, cs);
-        if (rc != 0) return rc;
+        if (rc != 0) {
+            join_internal();
+            return rc;
+        }
         ATTN_CK(cudaEventRecord(hp.comp_done[s], cs), "cudaEventRecord (compute)");
 
         ATTN_CK(cudaStreamWaitEvent(hp.out, hp.comp_done[s], 0), "wait (copy-out)");
