@@ -103,3 +103,26 @@ def test_host_forward_is_ordered_on_the_callers_stream(attn):
     s.synchronize()
     attn.check(attn.attn_device_status(), "device status")
     assert torch.equal(back.view(torch.int16), o_ref.view(torch.int16))
+
+
+def test_host_buffers_need_no_alignment(attn):
+    """Host tensors may start anywhere (here 2 bytes past a 16-byte boundary):
+    only the device workspace has an alignment rule."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N, d = 1, 4, 2, 333, 64
+    q, k, v = prefill_inputs(9, B, Hq, Hkv, N, d, dev)
+    o_dev, lse_dev = attn.forward(q, k, v, causal=True, scale=scale_of(d))
+
+    def odd(t):
+        flat = torch.empty(t.numel() + 1, dtype=t.dtype, pin_memory=True)
+        view = flat[1:].view(t.shape)
+        view.copy_(t.cpu())
+        return view
+
+    hq, hk, hv = odd(q), odd(k), odd(v)
+    o_h, lse_h = odd(torch.zeros_like(q)), torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=True)
+    assert hq.data_ptr() % 16 == 2 and o_h.data_ptr() % 16 == 2
+    attn.forward_host(hq, hk, hv, causal=True, scale=scale_of(d), kv_heads_per_chunk=1, out=(o_h, lse_h))
+    attn.check(attn.attn_device_status(), "device status")
+    assert torch.equal(o_h.view(torch.int16), o_dev.cpu().view(torch.int16))
+    assert torch.equal(lse_h, lse_dev.cpu())
