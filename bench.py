@@ -262,7 +262,7 @@ def run_gpu(args):
         "roofline": {"bound": "tensor", "achieved": round(per_gpu, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(per_gpu / peaks["bf16_tflops"], 4), "traffic": fwd_traffic,
-                     "peak_source": f"{peak_src} bf16 burst", "kernel": "fwd_kernel<128>"},
+                     "peak_source": f"{peak_src} bf16 burst", "kernel": "fwd_kernel<128, false>"},
         "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "us_per_step": round(dec_avg_s * 1e6, 2),
                    "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4), "hbm_peak_gbs": peaks["hbm_gbs"],
                    "bytes_per_step": dec_bytes, "traffic": dec_traffic},
