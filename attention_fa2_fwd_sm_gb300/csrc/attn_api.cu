@@ -299,6 +299,10 @@ static int splits_for(int B, int Hkv, int max_seqlen, int sms) {
     if (s > by_len) s = by_len;
     if (s > kMaxSplits) s = kMaxSplits;
     if (s < 1) s = 1;
+    // Long caches: double the splits while each keeps at least 4096 keys and
+    // the grid stays within four CTAs per SM (about 1.7 waves of two resident
+    // CTAs per SM); the split sweep measured that 1-3% faster.
+    while (2 * s <= kMaxSplits && max_seqlen / (2 * s) >= 4096 && ctas * 2 * s <= 4LL * sms) s *= 2;
     return int(s);
 }
 

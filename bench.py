@@ -46,9 +46,9 @@ MEASURED_TRAFFIC = {
             "bytes_by_n": {32768: 3233736960 + 1090045184, 8192: 805450496 + 251987968}},
     "decode": {"files": ["decode_sm103.cu", "sm103_ptx.cuh"],
                "sha256": "36aafa55e29c4da67d0c4eaa0986fdf0cc5872b11bfdd3c4927189e3ebe70d5f",
-               # GQA decode B=8 Hq=64 Hkv=8 d=128, 4 splits, captured at 8192 keys;
-               # the bytes scale with the keys streamed
-               "bytes_per_key": (268593920 + 3189248) / 8192.0, "batch": 8},
+               # GQA decode B=8 Hq=64 Hkv=8 d=128, 8 splits (the heuristic's count at
+               # 32K keys), captured at 32768 keys: bytes_per_key = bytes / keys
+               "bytes_per_key": (1073940736 + 4702976) / 32768.0, "batch": 8, "splits": 8},
 }
 
 
@@ -248,7 +248,8 @@ def run_gpu(args):
     fwd_traffic = (tf["bytes_by_n"].get(N) if (tf and B == 1 and H == 128 and d == 128 and not causal
                                               and args.order == "head_first") else None)
     td = measured_traffic("decode")
-    dec_traffic = (round(td["bytes_per_key"] * S * Bd / td["batch"]) if (td and splits == 4) else None)
+    dec_traffic = (round(td["bytes_per_key"] * S * Bd / td["batch"])
+                   if (td and splits == td["splits"] and Bd == td["batch"]) else None)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 3), "higher_is_better": True,

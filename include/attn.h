@@ -295,7 +295,8 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int d, int num_splits);
 
 /* Split count attn_decode uses when given num_splits <= 0: about 5/3 CTAs
  * per SM of the current device in all (B * Hkv * splits), no split shorter
- * than 512 keys, at most 256 splits.  Returns a value >= 1 (or a negative
+ * than 512 keys, at most 256 splits; then doubled while every split keeps at
+ * least 4096 keys and the grid stays within 4 CTAs per SM.  Returns a value >= 1 (or a negative
  * error code for bad arguments).  Queries the current device's SM count once. */
 int attn_decode_num_splits(int B, int Hq, int Hkv, int max_seqlen);
 
