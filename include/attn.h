@@ -171,9 +171,14 @@ size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d,
  *   NAIVE_HEAD_FIRST (the die-split order is forward-only).
  *   workspace: device memory of at least attn_bwd_workspace_bytes(B, Hq, N)
  *   bytes, 16-byte aligned; it receives lse * log2(e) and Delta per query row.
- * Three kernels run on `stream`: the Delta pre-pass, the dK/dV pass (one CTA
- * per 128 keys of a KV head) and the dQ pass (one CTA per 128 query rows).
- * Every output element is written once; results do not depend on the order.
+ * Three kernels run on `stream`: the Delta pre-pass, the dK/dV pass (units of
+ * 128 keys of one KV head) and the dQ pass (units of 256 query rows of one
+ * query head); the two main passes are persistent grids that take units in
+ * the tile order.  Under HEAD_FIRST a causal dK/dV pass runs windows of the
+ * fewest (batch, KV head) pairs whose key blocks cover the SMs three times,
+ * longest block first across the window, so that no head's long blocks start
+ * at the end of the launch.  Every output element is written once; results
+ * do not depend on the order.
  */
 int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
              const float *lse, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d,

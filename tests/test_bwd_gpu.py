@@ -101,6 +101,30 @@ def test_tile_orders_are_bit_identical(attn, causal):
             assert torch.equal(a, b), f"order {order}"
 
 
+def test_causal_dkdv_windows_with_a_partial_last_window(attn):
+    """Causal head-first dK/dV runs windows of (batch, KV head) pairs longest
+    first, sized to cover the SMs three times.  Seven KV heads with windows of
+    five leave a partial last window.  Every order computes each block the
+    same way, so the gradients equal block-first's bit for bit, and dV of each
+    KV head sums to the group's dO."""
+    dev = torch.device("cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nblk = -(-3 * sms // 5)
+    assert -(-3 * sms // nblk) == 5
+    B, Hq, Hkv, N, d = 1, 14, 7, nblk * 128 - 37, 64
+    G = Hq // Hkv
+    q, k, v = prefill_inputs(26, B, Hq, Hkv, N, d, dev)
+    dout = output_grad(26, B, Hq, N, d, dev)
+    got = _fwd_bwd(attn, q, k, v, dout, True, order=0)
+    ref = _fwd_bwd(attn, q, k, v, dout, True, order=1)
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    dv32 = got[2].float()
+    for g in range(Hkv):
+        want = dout[0, g * G:(g + 1) * G].float().sum((0, 1))
+        assert torch.allclose(dv32[0, g].sum(0), want, rtol=1e-2, atol=1e-2 * want.abs().max().item())
+
+
 def test_d56_equals_zero_padding_to_64(attn):
     dev = torch.device("cuda")
     B, H, N = 1, 4, 700
