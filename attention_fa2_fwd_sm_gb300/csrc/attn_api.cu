@@ -153,6 +153,9 @@ static int validate_fwd_sizes(int B, int Hq, int Hkv, int N, int d, float scale,
     if (d != 56 && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     // tensor-map limits: each dimension < 2^32, strides < 2^40 bytes
     if ((long long)B * Hq >= (1LL << 31) || (long long)N * d * 2 >= (1LL << 39)) return ATTN_ERR_ARG;
+    // The persistent forward and backward kernels take work units (at most
+    // B * Hq * ceil(N / 128) of them) from 32-bit counters.
+    if ((long long)B * Hq * ((N + 127) / 128) >= (1LL << 31)) return ATTN_ERR_ARG;
     return ATTN_OK;
 }
 

@@ -100,7 +100,9 @@ enum attn_tile_order {
  *   d in {56, 64, 128}; d = 56 is computed as 64 with zero columns, which
  *   gives the same result as explicit zero padding (scale stays as passed).
  *   causal != 0 keeps key j for query i iff j <= i.
- *   B, Hq, Hkv, N >= 1; Hq % Hkv == 0; scale > 0 and finite.
+ *   B, Hq, Hkv, N >= 1; Hq % Hkv == 0; scale > 0 and finite;
+ *   B * Hq * ceil(N / 128) < 2^31 (work units are handed out from 32-bit
+ *   counters; no call whose tensors fit in device memory comes near it).
  * Uses the HEAD_FIRST order.
  */
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,

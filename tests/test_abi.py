@@ -106,6 +106,7 @@ def _fwd(**kw):
     (dict(scale=float("nan")), attn.ATTN_ERR_ARG),
     (dict(tile_order=4), attn.ATTN_ERR_ARG),
     (dict(tile_order=-1), attn.ATTN_ERR_ARG),
+    (dict(B=1 << 16, Hq=256, Hkv=256, N=1 << 16), attn.ATTN_ERR_ARG),  # 2^33 work units
     (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
     (dict(d=32), attn.ATTN_ERR_UNSUPPORTED),
     (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
