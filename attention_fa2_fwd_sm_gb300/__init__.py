@@ -53,6 +53,7 @@ SIGNATURES = {
     "attn_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "attn_tile_map": (_I, [_I, _I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
     "attn_tile_map_die_split": (_I, [_I, _I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
+    "attn_bwd_tile_map": (_I, [_I, _I, _I, _I, _I, _I, _LL, _IP, _IP, _IP]),
     "attn_die_map": (_I, [_IP, _I, _FP]),
     "attn_fwd_units": (_LL, [_I, _I, _I]),
     "attn_device_status": (_I, [_P]),
@@ -221,6 +222,15 @@ def attn_tile_map_die_split(B, Hq, Hkv, N, causal, die, k):
         return None
     check(rc, "attn_tile_map_die_split")
     return b.value, h.value, m.value
+
+
+def attn_bwd_tile_map(tile_order, B, Hkv, N, causal, num_sms, unit):
+    """(b, g, j) of dK/dV unit `unit`: batch entry, KV head, 128-key block."""
+    b, g, j = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = lib().attn_bwd_tile_map(int(tile_order), B, Hkv, N, int(bool(causal)), int(num_sms), int(unit),
+                                 ctypes.byref(b), ctypes.byref(g), ctypes.byref(j))
+    check(rc, "attn_bwd_tile_map")
+    return b.value, g.value, j.value
 
 
 def attn_die_map(capacity=256):

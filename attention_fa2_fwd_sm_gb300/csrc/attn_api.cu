@@ -13,6 +13,7 @@
 
 #include "../../include/attn.h"
 #include "attn_internal.h"
+#include "dkdv_order.cuh"
 #include "tile_order.cuh"
 
 namespace attn {
@@ -137,6 +138,21 @@ int attn_tile_map_die_split(int B, int Hq, int Hkv, int N, int causal, int die, 
     *b = t.b;
     *h = t.h;
     *m = t.m;
+    return ATTN_OK;
+}
+
+int attn_bwd_tile_map(int tile_order, int B, int Hkv, int N, int causal, int num_sms, long long unit, int *b,
+                      int *g, int *j) {
+    if (!b || !g || !j || B <= 0 || Hkv <= 0 || N <= 0 || num_sms <= 0) return ATTN_ERR_ARG;
+    if (tile_order < kHeadFirst || tile_order > kNaiveHeadFirst) return ATTN_ERR_ARG;
+    if ((long long)B * Hkv >= (1LL << 31)) return ATTN_ERR_ARG;
+    const int nblk = (N + kKeyBlock - 1) / kKeyBlock;
+    if (unit < 0 || unit >= (long long)B * Hkv * nblk) return ATTN_ERR_ARG;
+    const KvTile t = dkdv_unit_to_tile(tile_order, unit, B, Hkv, nblk,
+                                       dkdv_window(tile_order, causal ? 1 : 0, B, Hkv, nblk, num_sms));
+    *b = t.b;
+    *g = t.g;
+    *j = t.j;
     return ATTN_OK;
 }
 

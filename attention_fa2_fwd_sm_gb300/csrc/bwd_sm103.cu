@@ -49,6 +49,7 @@
 
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
+#include "dkdv_order.cuh"
 #include "tile_order.cuh"
 
 namespace attn {
@@ -130,41 +131,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
 
 // ------------------------------------------------------------------ schedule
 
-constexpr int kKvWindowWaves = 3;
-
-// dkdv unit -> (b, kv head g, key block j).  Head-first: j fastest (causal:
-// ascending, so the blocks with the most query rows start first); with
-// kv_window = W > 1, W consecutive (b, g) pairs form a window whose units run
-// longest first across its pairs (j = r / W, pair = r % W), so a pair's long
-// blocks never wait for the end of the launch.  Block-first: (b, g) fastest.
-struct KvUnit {
-    int b, g, j;
-};
+// dkdv unit -> (b, kv head g, key block j): dkdv_unit_to_tile (the
+// scheduler header), with the launch's window.
+using KvUnit = KvTile;
 __device__ __forceinline__ KvUnit kv_unit(const Params &p, long long u) {
-    KvUnit w;
-    const int nbg = p.B * p.Hkv;
-    if (p.order == kBlockFirst) {
-        const int bg = int(u % nbg);
-        w.j = int(u / nbg);
-        w.b = bg / p.Hkv;
-        w.g = bg % p.Hkv;
-    } else if (p.kv_window > 1) {
-        const long long span = (long long)p.kv_window * p.nblk;  // units of a full window
-        const long long win = u / span;
-        const int first = int(win) * p.kv_window;                 // first (b, g) pair of the window
-        const int width = min(p.kv_window, nbg - first);          // pairs in this window
-        const long long r = u - win * span;
-        w.j = int(r / width);
-        const int bg = first + int(r % width);
-        w.b = bg / p.Hkv;
-        w.g = bg % p.Hkv;
-    } else {
-        w.j = int(u % p.nblk);
-        const long long bg = u / p.nblk;
-        w.g = int(bg % p.Hkv);
-        w.b = int(bg / p.Hkv);
-    }
-    return w;
+    return dkdv_unit_to_tile(p.order, u, p.B, p.Hkv, p.nblk, p.kv_window);
 }
 
 // The i-th unit of this CTA (naive head-first: the CTA's own index), or -1.
@@ -1146,20 +1117,13 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
     p.causal = a.causal ? 1 : 0;
     p.order = a.order;
     p.nblk = nblk;
-    // Causal dK/dV units differ in length (key block j is read by N - 128 j
-    // query rows), and with few key blocks per KV head a pair's longest block
-    // is a large part of an SM's share of the work: run the fewest (b, g)
-    // pairs whose blocks cover the SMs kKvWindowWaves times as one window,
-    // longest first across them.  A list-scheduling simulation of the
-    // persistent CTAs (152 SMs, unit time = query blocks + 1) gives GQA 64/8
-    // causal 8K 0.78 -> 0.94 of perfect balance and 16K 0.93 -> 0.98; long
-    // sequences keep one pair per window.
-    p.kv_window = 1;
-    if (a.order == kHeadFirst && a.causal) {
-        const long long nbg = (long long)a.B * a.Hkv;
-        const long long want = ((long long)kKvWindowWaves * a.num_sms + nblk - 1) / nblk;
-        p.kv_window = int(std::max(1LL, std::min(nbg, want)));
-    }
+    // Causal dK/dV units differ in length, and with few key blocks per KV
+    // head a pair's longest block is a large part of an SM's share of the
+    // work, so causal head-first runs windows of pairs longest first.  A
+    // list-scheduling simulation of the persistent CTAs (152 SMs, unit time =
+    // query blocks + 1) gives GQA 64/8 causal 8K 0.78 -> 0.94 of perfect
+    // balance and 16K 0.93 -> 0.98; long sequences keep one pair per window.
+    p.kv_window = dkdv_window(a.order, a.causal, a.B, a.Hkv, nblk, a.num_sms);
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_ns = a.wait_ns;

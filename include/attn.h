@@ -322,6 +322,15 @@ int attn_tile_map(int tile_order, int B, int Hq, int Hkv, int N, int causal, lon
 int attn_tile_map_die_split(int B, int Hq, int Hkv, int N, int causal, int die, long long k,
                             int *b, int *h, int *m);
 
+/* Host-side view of the backward's dK/dV scheduler (attn_bwd): unit `unit`,
+ * 0 <= unit < B * Hkv * ceil(N / 128), maps to (*b, *g, *j): batch entry, KV
+ * head and 128-key block.  num_sms is the SM count of the launch (the causal
+ * HEAD_FIRST window depends on it; attn_bwd uses the current device's).
+ * Orders 0-2.  Pure host code; the same function runs inside the kernel.
+ * Returns ATTN_OK or ATTN_ERR_ARG. */
+int attn_bwd_tile_map(int tile_order, int B, int Hkv, int N, int causal, int num_sms, long long unit,
+                      int *b, int *g, int *j);
+
 /* Which die each SM of the current device is on, as the die-split order uses
  * it.  On the first call for a device (or the first die-split launch) a short
  * calibration runs synchronously on the legacy default stream: one thread per

@@ -114,3 +114,50 @@ def die_split_sequence(die: int, batch: int, hq: int, hkv: int, nb: int, causal:
                 for r in range(nb):
                     out.append((b, h, nb - 1 - r if causal else r))
     return out
+
+
+KEY_BLOCK = 128    # keys per dK/dV unit
+WINDOW_WAVES = 3   # causal head-first dK/dV windows cover the SMs this many times
+
+
+def dkdv_window(order: int, causal: bool, batch: int, hkv: int, nblk: int, num_sms: int) -> int:
+    """(batch entry, KV head) pairs per window of the dK/dV order: under the
+    causal mask and head-first, the fewest pairs whose key blocks together
+    number at least WINDOW_WAVES * num_sms (at most every pair); one pair in
+    every other case.  The pages define no backward order; this and
+    ``dkdv_sequence`` are this library's reading of "head-first" for a pass
+    whose ACC is one (batch entry, KV head) pair."""
+    if order != HEAD_FIRST or not causal:
+        return 1
+    need = -(-(WINDOW_WAVES * num_sms) // nblk)
+    return max(1, min(batch * hkv, need))
+
+
+def dkdv_sequence(order: int, batch: int, hkv: int, n: int, causal: bool, num_sms: int):
+    """Every dK/dV unit (b, g, j) -- key block j of KV head g of batch entry
+    b -- in the order the persistent CTAs take them.
+
+    * block-first: key block by key block, all pairs inside each block;
+    * head-first and naive head-first: the pairs in windows of
+      ``dkdv_window`` consecutive pairs; inside a window, key block by key
+      block in increasing j (under the causal mask key block j is read by the
+      N - 128 j query rows after it, so this is longest first), the window's
+      pairs inside each block.  A window of one pair is plain head-first:
+      every block of a pair before the next pair."""
+    nblk = num_blocks(n, KEY_BLOCK)
+    pairs = [divmod(p, hkv) for p in range(batch * hkv)]
+    out = []
+    if order == BLOCK_FIRST:
+        for j in range(nblk):
+            for b, g in pairs:
+                out.append((b, g, j))
+        return out
+    if order not in (HEAD_FIRST, NAIVE_HEAD_FIRST):
+        raise ValueError("unknown order")
+    w = dkdv_window(order, causal, batch, hkv, nblk, num_sms)
+    for start in range(0, len(pairs), w):
+        window = pairs[start:start + w]
+        for j in range(nblk):
+            for b, g in window:
+                out.append((b, g, j))
+    return out

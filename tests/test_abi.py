@@ -60,6 +60,25 @@ def test_scheduler_matches_the_definitions(L, order, causal, B, H, Hkv, N):
                 == T.unit_to_tile(order, u, B, H, nb, causal, H // Hkv))
 
 
+@pytest.mark.parametrize("order", T.ORDERS)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hkv,N,sms", [(1, 8, 8192, 152), (1, 7, 11739, 152), (2, 3, 1000, 152),
+                                         (1, 8, 32768, 152), (3, 5, 3000, 8), (1, 1, 1, 152)])
+def test_dkdv_scheduler_matches_the_definition(L, order, causal, B, Hkv, N, sms):
+    seq = T.dkdv_sequence(order, B, Hkv, N, causal, sms)
+    for u, want in enumerate(seq):
+        assert attn.attn_bwd_tile_map(order, B, Hkv, N, causal, sms, u) == want
+    with pytest.raises(attn.AttnError):
+        attn.attn_bwd_tile_map(order, B, Hkv, N, causal, sms, len(seq))
+
+
+def test_dkdv_scheduler_rejects_bad_arguments(L):
+    for args in [(3, 1, 2, 256, True, 152, 0), (0, 1, 2, 256, True, 0, 0), (0, 0, 2, 256, True, 152, 0),
+                 (0, 1, 2, 256, True, 152, -1)]:
+        with pytest.raises(attn.AttnError):
+            attn.attn_bwd_tile_map(*args)
+
+
 def test_scheduler_rejects_bad_units(L):
     with pytest.raises(attn.AttnError):
         attn.attn_tile_map(0, 1, 2, 2, 256, False, 2)

@@ -151,3 +151,56 @@ def test_die_split_with_one_die_is_head_first(causal):
     B, Hq, Hkv, nb = 2, 6, 3, 4
     assert T.die_split_sequence(0, B, Hq, Hkv, nb, causal, dies=1) == [
         T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, causal, Hq // Hkv) for u in range(B * Hq * nb)]
+
+
+# ------------------------------------------------------- backward dK/dV order
+DKDV_SHAPES = [  # B, Hkv, N, num_sms
+    (1, 8, 8192, 152),     # window of all 8 heads
+    (1, 8, 16384, 152),    # windows of 4
+    (1, 7, 11739, 152),    # windows of 5: a partial last window
+    (2, 3, 1000, 152),     # pairs across batch entries, one window
+    (1, 8, 32768, 152),    # windows of 2
+    (1, 2, 200000, 152),   # long: one pair per window
+    (3, 5, 3000, 8),       # few SMs: windows of 1
+]
+
+
+@pytest.mark.parametrize("B,Hkv,N,sms", DKDV_SHAPES)
+@pytest.mark.parametrize("order", T.ORDERS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_dkdv_sequence_is_a_permutation(B, Hkv, N, sms, order, causal):
+    nblk = T.num_blocks(N, T.KEY_BLOCK)
+    seq = T.dkdv_sequence(order, B, Hkv, N, causal, sms)
+    assert sorted(seq) == [(b, g, j) for b in range(B) for g in range(Hkv) for j in range(nblk)]
+
+
+@pytest.mark.parametrize("B,Hkv,N,sms", DKDV_SHAPES)
+def test_causal_head_first_dkdv_windows(B, Hkv, N, sms):
+    """Each window holds the fewest consecutive pairs whose blocks number at
+    least three times the SMs (or every pair), and runs longest first: the
+    key block never decreases inside a window, and within one key block the
+    window's pairs appear in increasing order."""
+    nblk = T.num_blocks(N, T.KEY_BLOCK)
+    w = T.dkdv_window(T.HEAD_FIRST, True, B, Hkv, nblk, sms)
+    assert w == min(B * Hkv, max(1, -(-3 * sms // nblk)))
+    assert w * nblk >= min(3 * sms, B * Hkv * nblk)
+    assert w == 1 or (w - 1) * nblk < 3 * sms
+    seq = T.dkdv_sequence(T.HEAD_FIRST, B, Hkv, N, True, sms)
+    pos = 0
+    for start in range(0, B * Hkv, w):
+        width = min(w, B * Hkv - start)
+        part = seq[pos:pos + width * nblk]
+        pos += width * nblk
+        assert {b * Hkv + g for b, g, _ in part} == set(range(start, start + width))
+        assert [j for _, _, j in part] == sorted(j for _, _, j in part)
+        assert [b * Hkv + g for b, g, _ in part[:width]] == list(range(start, start + width))
+    # non-causal and the other orders never interleave pairs
+    assert T.dkdv_window(T.HEAD_FIRST, False, B, Hkv, nblk, sms) == 1
+    assert T.dkdv_window(T.NAIVE_HEAD_FIRST, True, B, Hkv, nblk, sms) == 1
+
+
+def test_dkdv_head_first_without_a_window_is_pair_major():
+    seq = T.dkdv_sequence(T.HEAD_FIRST, 2, 2, 300, False, 152)
+    assert seq == [(0, 0, 0), (0, 0, 1), (0, 0, 2), (0, 1, 0), (0, 1, 1), (0, 1, 2),
+                   (1, 0, 0), (1, 0, 1), (1, 0, 2), (1, 1, 0), (1, 1, 1), (1, 1, 2)]
+    assert T.dkdv_sequence(T.BLOCK_FIRST, 1, 2, 256, True, 152) == [(0, 0, 0), (0, 1, 0), (0, 0, 1), (0, 1, 1)]
