@@ -55,7 +55,7 @@ int current_num_sms() {
 
 bool aligned16(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-constexpr int kMaxSplits = 256;
+constexpr int kMaxSplits = kDecodeMaxSplits;
 constexpr int kDecodeMaxGroup = 16;
 
 }  // namespace
@@ -401,6 +401,7 @@ int attn_decode_varlen(const void *q, const void *kcache, const void *vcache, co
     a.varlen_target = varlen_target(sms);
     a.varlen_min_chunk = kVarlenMinChunk;
     a.wait_ns = (unsigned long long)g_wait_ns.load();
+    a.num_sms = sms;
     return decode_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -443,6 +444,7 @@ int attn_decode(const void *q, const void *kcache, const void *vcache, const int
     a.ws_o = need ? reinterpret_cast<float *>(workspace) : nullptr;
     a.ws_lse = need ? reinterpret_cast<float *>(reinterpret_cast<char *>(workspace) + o_bytes) : nullptr;
     a.wait_ns = (unsigned long long)g_wait_ns.load();
+    a.num_sms = current_num_sms();  // 0 if unknown: the base ring
     return decode_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -40,6 +40,7 @@ struct DecodeLaunch {
     float scale;
     float *ws_o, *ws_lse;  // partial outputs / log-sum-exps (used when splits > 1)
     unsigned long long wait_ns;
+    int num_sms = 0;       // SMs of the device (0: unknown); picks the ring depth
     // Varlen path (plan != null): work list, its capacity, and the chunk rule.
     int *plan = nullptr;
     int varlen_max_items = 0;
@@ -91,6 +92,9 @@ int bwd_launch(const BwdLaunch &a, cudaStream_t stream);
 
 // Size of the built-in scratch array used by attn_decode_noalloc.
 constexpr size_t kDecodeNoAllocScratchBytes = size_t(4) << 20;
+// Largest split count attn_decode accepts (the merge stages one lse per split
+// in shared memory).
+constexpr int kDecodeMaxSplits = 256;
 
 // Device address of that array on the current device (looked up on the
 // first call for each device).

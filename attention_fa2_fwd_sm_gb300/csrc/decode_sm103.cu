@@ -57,13 +57,21 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxGroup = 16;
 constexpr int kChunkGranule = 64;
 
+// K/V ring depth.  Three 32 KiB stages at d = 128 let two CTAs share an SM;
+// a grid of at most one CTA per SM (short batches, latency-bound) takes six,
+// twice the bytes in flight per CTA.
 template <int D>
+constexpr int kBaseStages = (D == 128) ? 3 : 6;
+template <int D>
+constexpr int kDeepStages = 6;
+
+template <int D, int S = kBaseStages<D>>
 struct Cfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kChunkBytes = kKeysPerStage * 128;      // 64 keys x 128 bytes
     static constexpr int kTileBytes = kKeysPerStage * D * 2;     // one K or V tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = (D == 128) ? 3 : 6;
+    static constexpr int kStages = S;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kCombineBytes = kConsumerWarps * (kMaxGroup * D + 2 * kMaxGroup) * 4;
     static constexpr int kDataBytes = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
@@ -124,11 +132,11 @@ __device__ __forceinline__ uint32_t mask_pair(uint32_t r, int k_lo, int n_valid)
     return r;
 }
 
-template <int D>
+template <int D, int S>
 __global__ void __launch_bounds__(kThreads)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const Params p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, S>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -386,19 +394,46 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // Merge: L = max_s lse_s, w_s = exp(lse_s - L), O = sum_s w_s O_s / sum_s w_s.
+// The block stages the lse values in shared memory (one load per thread) and
+// issues the partial outputs eight splits at a time, so the merge costs a few
+// memory round trips instead of one per split; the sums run over s in order.
 template <int D>
 __global__ void __launch_bounds__(D) merge_kernel(const float *ws_o, const float *ws_lse,
                                                   __nv_bfloat16 *o, int num_splits) {
+    __shared__ float lse_sh[kDecodeMaxSplits];
+    __shared__ float max_sh[D / 32];
     griddep_wait();  // launched behind the decode grid, which writes the partials
     const int bh = blockIdx.x, col = threadIdx.x;
     const float *lse = ws_lse + (size_t)bh * num_splits;
     const float *po = ws_o + (size_t)bh * num_splits * D;
     float L = -INFINITY;
-    for (int s = 0; s < num_splits; ++s) L = fmaxf(L, lse[s]);
+    for (int s = col; s < num_splits; s += D) {
+        const float v = lse[s];
+        lse_sh[s] = v;
+        L = fmaxf(L, v);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, off));
+    if ((col & 31) == 0) max_sh[col >> 5] = L;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) L = fmaxf(L, max_sh[w]);
     float wsum = 0.f, acc = 0.f;
     if (L != -INFINITY) {
-        for (int s = 0; s < num_splits; ++s) {
-            const float w = __expf(lse[s] - L);
+        int s = 0;
+        for (; s + 8 <= num_splits; s += 8) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = po[(size_t)(s + i) * D + col];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float w = __expf(lse_sh[s + i] - L);
+                wsum += w;
+                acc += w * v[i];
+            }
+        }
+        for (; s < num_splits; ++s) {
+            const float w = __expf(lse_sh[s] - L);
             wsum += w;
             acc += w * po[(size_t)s * D + col];
         }
@@ -516,9 +551,9 @@ cudaError_t launch_programmatic(void (*kernel)(KArgs...), dim3 grid, dim3 block,
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int D>
+template <int D, int S>
 int launch(const DecodeLaunch &a, cudaStream_t stream) {
-    using C = Cfg<D>;
+    using C = Cfg<D, S>;
     CUtensorMap mk, mv;
     if (!encode_bf16_3d(&mk, a.kcache, D, uint64_t(a.max_seqlen), uint64_t(a.B) * a.Hkv, 64,
                         kKeysPerStage) ||
@@ -544,7 +579,7 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
     const int dev = slot_for_device();
     if (dev < 0 || !attr_set[dev]) {
         const cudaError_t e = cudaFuncSetAttribute(
-            decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            decode_kernel<D, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(decode_kernel)");
         if (dev >= 0) attr_set[dev] = true;
     }
@@ -556,14 +591,14 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
                                                   a.varlen_min_chunk, a.plan);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return note_cuda_error(e, "varlen_plan_kernel launch");
-        e = launch_programmatic(decode_kernel<D>, dim3(a.Hkv, a.varlen_max_items, 1), dim3(kThreads),
+        e = launch_programmatic(decode_kernel<D, S>, dim3(a.Hkv, a.varlen_max_items, 1), dim3(kThreads),
                                 C::kSmemBytes, stream, mk, mv, p);
         if (e != cudaSuccess) return note_cuda_error(e, "decode_kernel launch (varlen)");
         e = launch_programmatic(merge_varlen_kernel<D>, dim3(a.B * a.Hq), dim3(D), 0, stream,
                                 (const int *)a.plan, a.B, a.Hq, (const float *)a.ws_o, (const float *)a.ws_lse, p.o);
         return e == cudaSuccess ? 0 : note_cuda_error(e, "merge_varlen_kernel launch");
     }
-    decode_kernel<D><<<dim3(a.num_splits, a.Hkv, a.B), dim3(kThreads), C::kSmemBytes, stream>>>(mk, mv, p);
+    decode_kernel<D, S><<<dim3(a.num_splits, a.Hkv, a.B), dim3(kThreads), C::kSmemBytes, stream>>>(mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return note_cuda_error(e, "decode_kernel launch");
     if (a.num_splits > 1) {
@@ -577,8 +612,12 @@ int launch(const DecodeLaunch &a, cudaStream_t stream) {
 }  // namespace dec
 
 int decode_launch(const DecodeLaunch &a, cudaStream_t stream) {
-    if (a.d == 64) return dec::launch<64>(a, stream);
-    return dec::launch<128>(a, stream);
+    // The split grid of at most one CTA per SM runs the deep ring; the varlen
+    // grid (an upper bound on its work items) keeps the base ring.
+    const bool deep = !a.plan && a.num_sms > 0 && (long long)a.num_splits * a.Hkv * a.B <= a.num_sms;
+    if (a.d == 64) return dec::launch<64, dec::kBaseStages<64>>(a, stream);
+    return deep ? dec::launch<128, dec::kDeepStages<128>>(a, stream)
+                : dec::launch<128, dec::kBaseStages<128>>(a, stream);
 }
 
 cudaError_t decode_noalloc_scratch(void **ptr) {
