@@ -320,6 +320,26 @@ def run_gpu(args):
                          "api": "attn_fwd_host (C ABI): pinned host buffers, copies overlapped with the"
                                 " kernels in chunks of KV heads"}
         result["gpu_launches_e2e"] = (reps + 1) * chunks
+        # The same bytes moved with no kernels, inputs in and outputs out on two
+        # streams as the pipeline overlaps them: when this approaches
+        # ms_per_step, the host link and not the kernels sets the pace.
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+        def copies():
+            with torch.cuda.stream(s_in):
+                for dst, src in ((q, hq_), (k, hk_), (v, hv_)):
+                    dst.copy_(src, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                ho.copy_(o, non_blocking=True)
+                hl.copy_(lse, non_blocking=True)
+
+        copies()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(2):
+            copies()
+        torch.cuda.synchronize(dev)
+        result["e2e"]["copy_only_ms"] = round((time.perf_counter() - t0) / 2 * 1e3, 3)
 
     if args.cpu_baseline and rank == 0:
         result["cpu_baseline"] = cpu_baseline(q, k, v, scale, causal, args.cpu_seconds)
