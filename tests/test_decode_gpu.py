@@ -83,6 +83,22 @@ def test_workspace_partials_match_the_oracle(attn, splits):
     assert_close(to64(o), m_ref, what="merged")
 
 
+def test_ring_depth_boundary(attn):
+    """A split grid of at most one CTA per SM runs the six-stage K/V ring, a
+    larger one the three-stage ring; both sides of the boundary match the
+    oracle (some of these splits are empty)."""
+    dev = torch.device("cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, Hq, Hkv, S, d = 1, 64, 8, 4000, 128
+    n = sms // Hkv  # n * Hkv CTAs fit one per SM; n + 1 do not
+    q, kc, vc = decode_inputs(52, B, Hq, Hkv, S, d, dev)
+    lens = [S - 3]
+    o_ref, _ = oracle.decode(to64(q), to64(kc), to64(vc), lens, scale_of(d))
+    for splits in (n, n + 1):
+        o, _, _ = _decode(attn, q, kc, vc, lens, splits)
+        assert_close(to64(o), o_ref, what=f"splits={splits} ({splits * Hkv} CTAs, {sms} SMs)")
+
+
 def test_split_counts_agree(attn):
     dev = torch.device("cuda")
     B, Hq, Hkv, S, d = 2, 64, 8, 5000, 128
