@@ -60,6 +60,9 @@ static __device__ int g_bwd_status;
 // {next unit, CTAs finished}; the last CTA of a launch resets its pair.
 constexpr int kBwdSchedSlots = 64;
 static __device__ unsigned int g_bwd_work[kBwdSchedSlots][2][2];
+// Launch sequence number behind the slot choice: one counter for both head
+// dimensions, since their launches share g_bwd_work.
+static std::atomic<unsigned int> g_bwd_launch_seq{0};
 
 namespace bwd {
 
@@ -1102,8 +1105,6 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(backward kernels)");
         if (dev >= 0) attr_set[dev] = true;
     }
-    static std::atomic<unsigned int> launch_seq{0};
-
     Params p;
     p.lse2 = lse2;
     p.delta = delta;
@@ -1127,7 +1128,7 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_ns = a.wait_ns;
-    p.sched_slot = int(launch_seq.fetch_add(1) % kBwdSchedSlots);
+    p.sched_slot = int(g_bwd_launch_seq.fetch_add(1) % kBwdSchedSlots);
 
     // dK, dV
     p.out0 = reinterpret_cast<__nv_bfloat16 *>(a.dk);

@@ -55,6 +55,9 @@ static __device__ int g_fwd_status;
 constexpr int kSchedSlots = 64;
 constexpr int kWorkDone = 2;
 static __device__ unsigned int g_fwd_work[kSchedSlots][4];
+// Launch sequence number behind the slot choice: one counter for every
+// instantiation, since they all share g_fwd_work.
+static std::atomic<unsigned int> g_fwd_launch_seq{0};
 
 namespace fwd {
 
@@ -653,8 +656,7 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
     p.total_units = (long long)a.B * a.Hq * p.nb;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_ns = a.wait_ns;
-    static std::atomic<unsigned int> launch_seq{0};
-    p.sched_slot = int(launch_seq.fetch_add(1) % kSchedSlots);
+    p.sched_slot = int(g_fwd_launch_seq.fetch_add(1) % kSchedSlots);
     p.die_of_sm = nullptr;
     if (a.order == kDieSplitHeadFirst) {
         const int rc = die_map_device(&p.die_of_sm);

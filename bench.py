@@ -40,10 +40,10 @@ DEC = dict(B=8, Hq=64, Hkv=8, S=32768, d=128)
 # digest; after any change to them the bench reports null until re-captured.
 MEASURED_TRAFFIC = {
     "fwd": {"files": ["fwd_sm103.cu", "sm103_ptx.cuh", "tile_order.cuh"],
-            "sha256": "6225aea524f735f54e261ef0cd1156a8743e1582d01f5180446998bb68dc6b5a",
+            "sha256": "6941f2c90f2f9fd297d4fa680bd15435239464c3eb0d1a5bbb847666e984ee3b",
             # MHA B=1 H=128 d=128, head-first, captured at N=32768 and N=8192 (one-pass
             # capture of dram__bytes_read.sum + dram__bytes_write.sum)
-            "bytes_by_n": {32768: 3233736960 + 1090045184, 8192: 805450496 + 251987968}},
+            "bytes_by_n": {32768: 3235301376 + 1087528704, 8192: 805625088 + 250836992}},
     "decode": {"files": ["decode_sm103.cu", "sm103_ptx.cuh"],
                "sha256": "eea28fbd34c4bacf564487ff290b51fa5037287fc8703873f7b0f1aabac57512",
                # GQA decode B=8 Hq=64 Hkv=8 d=128, 8 splits (the heuristic's count at

@@ -125,6 +125,38 @@ def test_causal_dkdv_windows_with_a_partial_last_window(attn):
         assert torch.allclose(dv32[0, g].sum(0), want, rtol=1e-2, atol=1e-2 * want.abs().max().item())
 
 
+def test_concurrent_launches_of_both_head_dims(attn):
+    """Backward launches of both head dimensions draw their scheduler slots
+    from one sequence, so launches running at once on two streams never share
+    a slot: every gradient equals that of a launch run alone."""
+    dev = torch.device("cuda")
+    B, H, N = 1, 4, 1024
+    data = {}
+    for d in (64, 128):
+        q, k, v = prefill_inputs(60 + d, B, H, H, N, d, dev)
+        dout = output_grad(60 + d, B, H, N, d, dev)
+        o, lse = attn.forward(q, k, v, causal=True)
+        data[d] = (q, k, v, o, lse, dout)
+    ref = {d: attn.backward(*data[d], causal=True) for d in data}
+    torch.cuda.synchronize()
+    nbytes = attn.attn_bwd_workspace_bytes(B, H, N)
+    streams = {d: torch.cuda.Stream() for d in data}
+    runs = []
+    for _ in range(6):
+        for d in data:
+            q, k, v, o, lse, dout = data[d]
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+            attn.check(attn.attn_bwd(q, k, v, o, dout, lse, *grads, B, H, H, N, d, d ** -0.5, True, 0, ws,
+                                     nbytes, streams[d].cuda_stream), "attn_bwd")
+            runs.append((d, grads, ws))
+    torch.cuda.synchronize()
+    attn.check(attn.attn_device_status(), "device status")
+    for d, grads, _ in runs:
+        for a, b in zip(grads, ref[d]):
+            assert torch.equal(a, b), f"d={d}"
+
+
 def test_d56_equals_zero_padding_to_64(attn):
     dev = torch.device("cuda")
     B, H, N = 1, 4, 700

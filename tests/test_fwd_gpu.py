@@ -144,6 +144,29 @@ def test_repeated_calls_are_deterministic(attn):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+def test_concurrent_launches_of_both_head_dims(attn):
+    """Forward launches of every head dimension draw their scheduler slots
+    from one sequence, so launches running at once on two streams never share
+    a slot: every output equals that of a launch run alone."""
+    dev = torch.device("cuda")
+    B, H, N = 1, 8, 2048
+    ins = {d: prefill_inputs(40 + d, B, H, H, N, d, dev) for d in (64, 128)}
+    ref = {d: _run(attn, *ins[d], False, scale_of(d))[0] for d in ins}
+    streams = {d: torch.cuda.Stream() for d in ins}
+    outs = {d: [torch.empty_like(ref[d]) for _ in range(8)] for d in ins}
+    torch.cuda.synchronize()
+    for i in range(8):
+        for d in ins:
+            q, k, v = ins[d]
+            attn.check(attn.attn_fwd(q, k, v, outs[d][i], None, B, H, H, N, d, scale_of(d), False,
+                                     streams[d].cuda_stream), "attn_fwd")
+    torch.cuda.synchronize()
+    attn.check(attn.attn_device_status(), "device status")
+    for d in ins:
+        for o in outs[d]:
+            assert torch.equal(o, ref[d]), f"d={d}"
+
+
 def test_no_lse_and_no_write_past_the_output(attn):
     """lse may be NULL; the output is written only inside its rows."""
     dev = torch.device("cuda")
