@@ -57,6 +57,10 @@ SMALL = [
     (1, 4, 2, 385, 64, True),
     (2, 2, 1, 577, 56, True),
     (1, 2, 2, 767, 64, False),
+    # more units than SMs: several units per persistent CTA, causal GQA ACCs
+    # spanning batch entries, and the DeepSeek-like head dimension
+    (3, 32, 8, 600, 128, True),
+    (2, 16, 16, 1100, 56, True),
 ]
 
 
