@@ -83,6 +83,29 @@ def test_workspace_partials_match_the_oracle(attn, splits):
     assert_close(to64(o), m_ref, what="merged")
 
 
+def test_split_heuristic_follows_its_rule(attn):
+    """attn_decode_num_splits restated from its header: round(floor(5 SMs / 3)
+    / (B Hkv)), capped by floor(S / 512) and by 256, at least 1; then doubled
+    while every split keeps at least 4096 keys and the grid stays within four
+    CTAs per SM.  On a 152-SM GB300 it gives the counts the split sweep
+    measured for the decode configurations."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def rule(B, Hkv, S):
+        ctas = B * Hkv
+        s = max(1, min((5 * sms // 3 + ctas // 2) // ctas, S // 512, 256))
+        while 2 * s <= 256 and S // (2 * s) >= 4096 and ctas * 2 * s <= 4 * sms:
+            s *= 2
+        return s
+
+    for B in (1, 2, 8, 32, 300):
+        for S in (1, 511, 4096, 8192, 32768, 131072, 1 << 20):
+            assert attn.attn_decode_num_splits(B, 64, 8, S) == rule(B, 8, S), (B, S)
+    if sms == 152:
+        got = [attn.attn_decode_num_splits(B, 64, 8, S) for B in (1, 8, 32) for S in (8192, 32768, 131072)]
+        assert got == [16, 32, 32, 4, 8, 8, 2, 2, 2]
+
+
 def test_ring_depth_boundary(attn):
     """A split grid of at most one CTA per SM runs the six-stage K/V ring, a
     larger one the three-stage ring; both sides of the boundary match the
