@@ -619,6 +619,41 @@ def run_bwd_one(args):
                       "launches_per_call": 3, "calls": args.warmup + args.steps}), flush=True)
 
 
+def run_decode_one(args):
+    """GQA decode (Hq=64, Hkv=8, d=128) of one batch size and KV length with
+    the heuristic's split count (or --dec-splits): W warm-up calls, then K
+    timed calls (median), the L2 flushed before each; one JSON line."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import decode_inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    flush = _l2_flush_buffer(torch, dev)
+    stream = torch.cuda.current_stream(dev)
+    Hq, Hkv, d = DEC["Hq"], DEC["Hkv"], DEC["d"]
+    B, S = args.dec_batch, args.dec_len
+    q, kc, vc = decode_inputs(70, B, Hq, Hkv, S, d, dev)
+    seqlens = torch.full((B,), S, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    sp = args.dec_splits if args.dec_splits > 0 else attn.attn_decode_num_splits(B, Hq, Hkv, S)
+    wb = attn.attn_decode_workspace_bytes(B, Hq, d, sp)
+    ws = torch.empty(max(wb, 16), dtype=torch.uint8, device=dev)
+    fn = lambda: attn.check(attn.attn_decode(q, kc, vc, seqlens, o, B, Hq, Hkv, d, d ** -0.5, sp, S, ws, wb,
+                                             stream.cuda_stream), "decode")
+    for _ in range(args.warmup):
+        fn()
+    ms = _time_calls(torch, fn, args.steps, flush, stream)
+    nbytes = 2 * B * Hkv * S * d * 2 + 2 * B * Hq * d * 2
+    gbs = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({"mode": "decode-one", "B": B, "S": S, "Hq": Hq, "Hkv": Hkv, "d": d, "splits": sp,
+                      "us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                      "l2": "flushed before every call"}), flush=True)
+
+
 def run_decode_varlen(args):
     """Ragged multi-user decode batches (GQA Hq=64, Hkv=8, d=128): attn_decode
     (split count from max_seqlen) against attn_decode_varlen (chunks from the
@@ -737,8 +772,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--mode", default="step",
-                    choices=["step", "decode-sweep", "decode-varlen", "fwd-sweep", "fwd-one", "bwd-one",
-                             "bwd-sweep", "die-map"],
+                    choices=["step", "decode-sweep", "decode-one", "decode-varlen", "fwd-sweep", "fwd-one",
+                             "bwd-one", "bwd-sweep", "die-map"],
                     help="step: the contract's one-line benchmark; the sweeps print one line "
                          "per configuration; fwd-one times one forward configuration")
     ap.add_argument("--batch", type=int, default=1, help="fwd-one: batch")
@@ -755,6 +790,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--dec-batch", type=int, default=DEC["B"], help="decode batch")
     ap.add_argument("--dec-len", type=int, default=DEC["S"], help="decode cached keys per sequence")
+    ap.add_argument("--dec-splits", type=int, default=0, help="decode-one: split count (0: the heuristic's)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=8.0)
     args = ap.parse_args()
@@ -769,6 +805,8 @@ def main():
         return run_die_map(args)
     if args.mode == "bwd-one":
         return run_bwd_one(args)
+    if args.mode == "decode-one":
+        return run_decode_one(args)
     if args.mode == "decode-varlen":
         return run_decode_varlen(args)
     if args.mode == "bwd-sweep":
