@@ -43,6 +43,8 @@ SIGNATURES = {
     "attn_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ, _P]),
     "attn_fwd_host_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_fwd_host_trace": (_I, [_I]),
+    "attn_fwd_host_trace_read": (_LL, [_FP, _LL]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
@@ -136,6 +138,25 @@ def attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, 
 
 def attn_fwd_host_workspace_bytes(B, Hq, Hkv, N, d, kv_heads_per_chunk=0) -> int:
     return int(lib().attn_fwd_host_workspace_bytes(B, Hq, Hkv, N, d, kv_heads_per_chunk))
+
+
+def attn_fwd_host_trace(enable) -> int:
+    return int(lib().attn_fwd_host_trace(int(bool(enable))))
+
+
+def attn_fwd_host_trace_read(capacity=None):
+    """Per-chunk timeline of the last traced attn_fwd_host call on the current
+    device: a list of (copy-in done, kernel reached, kernel done, copy-out
+    done) in ms from the call's start.  Raises when there is none."""
+    n = int(lib().attn_fwd_host_trace_read(None, 0))
+    if n < 0:
+        check(n, "attn_fwd_host_trace_read")
+    cap = n if capacity is None else min(n, int(capacity))
+    buf = (ctypes.c_float * (4 * max(cap, 1)))()
+    got = int(lib().attn_fwd_host_trace_read(buf, cap))
+    if got < 0:
+        check(got, "attn_fwd_host_trace_read")
+    return [tuple(buf[4 * c: 4 * c + 4]) for c in range(cap)]
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, tile_order,

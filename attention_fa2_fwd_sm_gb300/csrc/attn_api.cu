@@ -249,6 +249,14 @@ int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *l
     return fwd_host_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int attn_fwd_host_trace(int enable) { return fwd_host_trace(enable); }
+
+long long attn_fwd_host_trace_read(float *ms, long long capacity) {
+    if (capacity < 0 || (capacity > 0 && !ms)) return ATTN_ERR_ARG;
+    const long long n = fwd_host_trace_read(ms, capacity);
+    return n == -1 ? ATTN_ERR_ARG : n;
+}
+
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
              int Hkv, int N, int d, float scale, int causal, attn_stream_t stream) {
     return attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, ATTN_ORDER_HEAD_FIRST,

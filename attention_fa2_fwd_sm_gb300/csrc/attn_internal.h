@@ -69,6 +69,11 @@ struct HostChunkLayout {
 HostChunkLayout host_chunk_layout(int Hq, int Hkv, int N, int d, int kv_heads_per_chunk);
 int host_default_chunk(int Hq, int Hkv, int N);
 int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream);
+// Per-chunk timeline of fwd_host_launch on the current device (see
+// attn_fwd_host_trace in attn.h).  fwd_host_trace_read returns the chunk count
+// of the last traced call, -1 when there is none, or an ATTN_ERR_* code.
+int fwd_host_trace(int enable);
+long long fwd_host_trace_read(float *ms, long long capacity);
 
 // Kernel attributes (the dynamic shared-memory limit) belong to the current
 // device, so the launchers set them once per device: slot_for_device()

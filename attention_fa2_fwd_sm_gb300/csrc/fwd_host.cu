@@ -20,6 +20,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "attn_internal.h"
 
@@ -38,6 +39,30 @@ struct HostPipe {
 
 HostPipe g_pipe[kMaxDevices];
 std::mutex g_pipe_mu;  // one call enqueues at a time (the streams and events are shared)
+
+// Per-chunk timeline of the last traced call on a device: ev[0] is recorded
+// on the caller's stream when the call starts, then four events per chunk
+// (copy-in done, kernel reached, kernel done, copy-out done).  Timing events
+// are recorded only while tracing is on.
+constexpr int kTracePerChunk = 4;
+struct HostTrace {
+    bool on = false;
+    bool valid = false;  // a traced call has been enqueued since tracing was enabled
+    long long chunks = 0;
+    std::vector<cudaEvent_t> ev;
+};
+HostTrace g_trace[kMaxDevices];
+
+cudaError_t trace_reserve(HostTrace &tr, long long chunks) {
+    const size_t need = size_t(1 + kTracePerChunk * chunks);
+    while (tr.ev.size() < need) {
+        cudaEvent_t e;
+        const cudaError_t rc = cudaEventCreate(&e);
+        if (rc != cudaSuccess) return rc;
+        tr.ev.push_back(e);
+    }
+    return cudaSuccess;
+}
 
 cudaError_t pipe_init(HostPipe &hp) {
     if (hp.ready) return cudaSuccess;
@@ -121,6 +146,16 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
         }                                                     \
     } while (0)
 
+    HostTrace &tr = g_trace[dev];
+    const bool tracing = tr.on;
+    if (tracing) {
+        tr.valid = false;
+        ATTN_CK(trace_reserve(tr, chunks), "cudaEventCreate (host forward trace)");
+        ATTN_CK(cudaEventRecord(tr.ev[0], stream), "cudaEventRecord (trace)");
+    }
+    auto trace_mark = [&](long long c, int k, cudaStream_t s) {
+        return tracing ? cudaEventRecord(tr.ev[size_t(1 + kTracePerChunk * c + k)], s) : cudaSuccess;
+    };
     ATTN_CK(cudaEventRecord(hp.start, stream), "cudaEventRecord (host forward)");
     for (cudaStream_t s : {hp.in, hp.comp, hp.out})
         ATTN_CK(cudaStreamWaitEvent(s, hp.start, 0), "cudaStreamWaitEvent (host forward)");
@@ -141,6 +176,7 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
         ATTN_CK(cudaMemcpyAsync(slot + L.k_off, hk + kv_at, kv_bytes, cudaMemcpyHostToDevice, hp.in), "copy k");
         ATTN_CK(cudaMemcpyAsync(slot + L.v_off, hv + kv_at, kv_bytes, cudaMemcpyHostToDevice, hp.in), "copy v");
         ATTN_CK(cudaEventRecord(hp.in_done[s], hp.in), "cudaEventRecord (copy-in)");
+        ATTN_CK(trace_mark(c, 0, hp.in), "cudaEventRecord (trace)");
 
         cudaStream_t cs = (s == 0) ? stream : hp.comp;
         ATTN_CK(cudaStreamWaitEvent(cs, hp.in_done[s], 0), "wait (compute)");
@@ -154,12 +190,14 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
         f.B = 1;
         f.Hq = hn;
         f.Hkv = gn;
+        ATTN_CK(trace_mark(c, 1, cs), "cudaEventRecord (trace)");
         const int rc = fwd_launch(f, cs);
         if (rc != 0) {
             join_internal();
             return rc;
         }
         ATTN_CK(cudaEventRecord(hp.comp_done[s], cs), "cudaEventRecord (compute)");
+        ATTN_CK(trace_mark(c, 2, cs), "cudaEventRecord (trace)");
 
         ATTN_CK(cudaStreamWaitEvent(hp.out, hp.comp_done[s], 0), "wait (copy-out)");
         ATTN_CK(cudaMemcpyAsync(ho + q_at, slot + L.o_off, q_bytes, cudaMemcpyDeviceToHost, hp.out), "copy o");
@@ -168,11 +206,51 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
                                     cudaMemcpyDeviceToHost, hp.out),
                     "copy lse");
         ATTN_CK(cudaEventRecord(hp.out_done[s], hp.out), "cudaEventRecord (copy-out)");
+        ATTN_CK(trace_mark(c, 3, hp.out), "cudaEventRecord (trace)");
+    }
+    if (tracing) {
+        tr.chunks = chunks;
+        tr.valid = true;
     }
     ATTN_CK(cudaEventRecord(hp.end, hp.out), "cudaEventRecord (host forward end)");
     ATTN_CK(cudaStreamWaitEvent(stream, hp.end, 0), "cudaStreamWaitEvent (host forward end)");
 #undef ATTN_CK
     return 0;
+}
+
+int fwd_host_trace(int enable) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return note_cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return note_cuda_error(cudaErrorInvalidDevice, "device index");
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    g_trace[dev].on = enable != 0;
+    g_trace[dev].valid = false;
+    return 0;
+}
+
+long long fwd_host_trace_read(float *ms, long long capacity) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return note_cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return note_cuda_error(cudaErrorInvalidDevice, "device index");
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostTrace &tr = g_trace[dev];
+    if (!tr.valid) return -1;
+    const long long n = tr.chunks;
+    // The copy-out stream's last event follows every other event of the call.
+    if ((e = cudaEventSynchronize(tr.ev[size_t(kTracePerChunk * n)])) != cudaSuccess)
+        return note_cuda_error(e, "cudaEventSynchronize (trace)");
+    const long long m = std::min(n, capacity);
+    for (long long c = 0; c < m; ++c)
+        for (int k = 0; k < kTracePerChunk; ++k) {
+            float t = 0.f;
+            if ((e = cudaEventElapsedTime(&t, tr.ev[0], tr.ev[size_t(1 + kTracePerChunk * c + k)])) !=
+                cudaSuccess)
+                return note_cuda_error(e, "cudaEventElapsedTime (trace)");
+            ms[kTracePerChunk * c + k] = t;
+        }
+    return n;
 }
 
 }  // namespace attn

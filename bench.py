@@ -1,13 +1,13 @@
 """Benchmark of the attention hot path on GB300 (one JSON line on stdout).
 
 A step is one pass of the whole hot path over one batch of synthetic input:
-one forward (prefill) call on the MHA workload (B=1, H=128, d=128,
-N=32768, non-causal, head-first order) and one split-KV decode call on the
-GQA decode workload (B=8, Hq=64, Hkv=8, d=128, 32768 cached keys per
-sequence).  ``value`` is the forward TFLOP/s (4*B*H*N^2*d algorithmic flops
-per call / the call's CUDA-event time); the decode figures are reported in
-the ``decode`` object.  Inputs are larger than L2 (4 GiB and 1 GiB), so no
-flush is needed between steps.
+one forward (prefill) call on the largest MHA workload (B=1, H=128, d=128,
+N=131072, non-causal, head-first order) and one split-KV decode call on the
+largest GQA decode workload (B=32, Hq=64, Hkv=8, d=128, 131072 cached keys
+per sequence).  ``value`` is the forward TFLOP/s (4*B*H*N^2*d algorithmic
+flops per call / the call's CUDA-event time); the decode figures are
+reported in the ``decode`` object.  Inputs are larger than L2 (16 GiB and
+17 GB), so no flush is needed between steps.
 
 ``--impl reference`` times the fp64 CPU oracle instead (on a bounded sample
 of the same forward workload: a number of query rows of one head), reported
@@ -30,25 +30,32 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s (% BF16 peak); GQA decode KV GB/s (% HBM) and us/step"
-FWD = dict(B=1, H=128, N=32768, d=128, causal=False)
-DEC = dict(B=8, Hq=64, Hkv=8, S=32768, d=128)
+FWD = dict(B=1, H=128, N=131072, d=128, causal=False)
+DEC = dict(B=32, Hq=64, Hkv=8, S=131072, d=128)
 
 
 # DRAM bytes (read + write) per launch measured with ncu for the kernels as
 # they stand in the listed sources (profiles/ holds the summaries and the
-# commands).  A value is reported only while the sources hash to the same
-# digest; after any change to them the bench reports null until re-captured.
+# commands).  Each capture is one launch of a reduced case of the bench's
+# workload -- fewer query heads at the same N for the forward, fewer
+# sequences at the same cache length and split count for decode -- and is
+# scaled to the bench's launch by the units it processes (heads, sequences):
+# each head's K/V stream and each sequence's cache are read independently of
+# the others, so the traffic grows in proportion.  A value is reported only
+# while the sources hash to the recorded digest; after any change to them the
+# bench reports null until re-captured.
 MEASURED_TRAFFIC = {
     "fwd": {"files": ["fwd_sm103.cu", "sm103_ptx.cuh", "tile_order.cuh"],
-            "sha256": "6941f2c90f2f9fd297d4fa680bd15435239464c3eb0d1a5bbb847666e984ee3b",
-            # MHA B=1 H=128 d=128, head-first, captured at N=32768 and N=8192 (one-pass
-            # capture of dram__bytes_read.sum + dram__bytes_write.sum)
-            "bytes_by_n": {32768: 3235301376 + 1087528704, 8192: 805625088 + 250836992}},
+            "sha256": None,
+            # MHA B=1 d=128 non-causal, head-first, H = Hq = Hkv = 16 at N = 131072
+            # (one-pass capture of dram__bytes_read.sum + dram__bytes_write.sum)
+            "capture": {"B": 1, "H": 16, "N": 131072, "d": 128, "causal": False,
+                        "order": "head_first", "bytes": None}},
     "decode": {"files": ["decode_sm103.cu", "sm103_ptx.cuh"],
-               "sha256": "eea28fbd34c4bacf564487ff290b51fa5037287fc8703873f7b0f1aabac57512",
-               # GQA decode B=8 Hq=64 Hkv=8 d=128, 8 splits (the heuristic's count at
-               # 32K keys), captured at 32768 keys: bytes_per_key = bytes / keys
-               "bytes_per_key": (1073906944 + 4580864) / 32768.0, "batch": 8, "splits": 8},
+               "sha256": None,
+               # GQA decode Hq=64 Hkv=8 d=128, B=4 sequences of 131072 keys, 2 splits
+               # (the heuristic's count at B=32), decode kernel only
+               "capture": {"B": 4, "S": 131072, "splits": 2, "bytes": None}},
 }
 
 
@@ -57,11 +64,31 @@ def measured_traffic(kind):
     unchanged since the capture, else None."""
     import hashlib
     entry = MEASURED_TRAFFIC[kind]
+    if entry["sha256"] is None or entry["capture"]["bytes"] is None:
+        return None
     h = hashlib.sha256()
     for f in entry["files"]:
         with open(os.path.join(ROOT, "attention_fa2_fwd_sm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    return entry if h.hexdigest() == entry["sha256"] else None
+    return entry["capture"] if h.hexdigest() == entry["sha256"] else None
+
+
+def fwd_traffic(B, H, N, d, causal, order):
+    """DRAM bytes per forward launch of an MHA problem (Hq = Hkv = H), scaled
+    from the reduced-head capture by B * H; None when no capture applies."""
+    c = measured_traffic("fwd")
+    if not c or (N, d, bool(causal), order) != (c["N"], c["d"], c["causal"], c["order"]):
+        return None
+    return round(c["bytes"] * (B * H) / (c["B"] * c["H"]))
+
+
+def decode_traffic(B, S, splits):
+    """DRAM bytes per decode-kernel launch, scaled from the reduced-batch
+    capture by B; None when no capture applies."""
+    c = measured_traffic("decode")
+    if not c or (S, splits) != (c["S"], c["splits"]):
+        return None
+    return round(c["bytes"] * B / c["B"])
 
 
 def fwd_flops(B, H, N, d, causal):
@@ -244,12 +271,8 @@ def run_gpu(args):
     dec_avg_s = dec_sum / K / 1e3
     dec_gbs = dec_bytes / dec_avg_s / 1e9
 
-    tf = measured_traffic("fwd")
-    fwd_traffic = (tf["bytes_by_n"].get(N) if (tf and B == 1 and H == 128 and d == 128 and not causal
-                                              and args.order == "head_first") else None)
-    td = measured_traffic("decode")
-    dec_traffic = (round(td["bytes_per_key"] * S * Bd / td["batch"])
-                   if (td and splits == td["splits"] and Bd == td["batch"]) else None)
+    fwd_bytes = fwd_traffic(B, H, N, d, causal, args.order)
+    dec_traffic = decode_traffic(Bd, S, splits)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 3), "higher_is_better": True,
@@ -262,8 +285,11 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (no flush)"},
         "roofline": {"bound": "tensor", "achieved": round(per_gpu, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(per_gpu / peaks["bf16_tflops"], 4), "traffic": fwd_traffic,
-                     "peak_source": f"{peak_src} bf16 burst", "kernel": "fwd_kernel<128, false>"},
+                     "frac": round(per_gpu / peaks["bf16_tflops"], 4), "traffic": fwd_bytes,
+                     "peak_source": f"{peak_src} bf16 burst", "kernel": "fwd_kernel<128, false>",
+                     "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch "
+                                        "with fewer heads at the same N, scaled by the head count"
+                                        if fwd_bytes else None)},
         "decode": {"value": round(dec_gbs, 1), "unit": "GB/s", "us_per_step": round(dec_avg_s * 1e6, 2),
                    "frac_hbm": round(dec_gbs / peaks["hbm_gbs"], 4), "hbm_peak_gbs": peaks["hbm_gbs"],
                    "bytes_per_step": dec_bytes, "traffic": dec_traffic},
@@ -277,7 +303,7 @@ def run_gpu(args):
         for name, oid in attn.ORDERS.items():
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, H, H, N, d, scale, causal, oid, sh), "warm")
-            reps = 3
+            reps = 2 if N >= 131072 else 3
             e0.record(stream)
             for _ in range(reps):
                 attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, H, H, N, d, scale, causal, oid, sh), "abl")
@@ -286,8 +312,8 @@ def run_gpu(args):
             ms = e0.elapsed_time(e1) / reps
             abl[name] = {"ms": round(ms, 3), "tflops": round(flops / (ms / 1e3) / 1e12, 2)}
         result["ablation"] = abl
-        # 1 warm-up + 3 timed launches per order (plus the die map's one-off probe)
-        result["gpu_launches_ablation"] = 4 * len(attn.ORDERS)
+        # 1 warm-up + the timed launches per order (plus the die map's one-off probe)
+        result["gpu_launches_ablation"] = (1 + reps) * len(attn.ORDERS)
 
     # -- end to end through the C ABI with host buffers --
     if args.e2e and rank == 0:
@@ -339,7 +365,17 @@ def run_gpu(args):
         for _ in range(2):
             copies()
         torch.cuda.synchronize(dev)
-        result["e2e"]["copy_only_ms"] = round((time.perf_counter() - t0) / 2 * 1e3, 3)
+        copy_ms = (time.perf_counter() - t0) / 2 * 1e3
+        result["e2e"]["copy_only_ms"] = round(copy_ms, 3)
+        # One more call with the library's per-chunk timeline switched on.
+        attn.check(attn.attn_fwd_host_trace(1), "trace on")
+        try:
+            e2e_step()
+            timeline = attn.attn_fwd_host_trace_read()
+        finally:
+            attn.check(attn.attn_fwd_host_trace(0), "trace off")
+        result["e2e"]["timeline"] = timeline_summary(timeline, copy_ms)
+        result["gpu_launches_e2e"] += chunks
 
     if args.cpu_baseline and rank == 0:
         result["cpu_baseline"] = cpu_baseline(q, k, v, scale, causal, args.cpu_seconds)
@@ -348,6 +384,36 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return result if rank == 0 else None
+
+
+def timeline_summary(tl, copy_only_ms):
+    """Summary of an attn_fwd_host timeline (per chunk: copy-in done, kernel
+    reached, kernel done, copy-out done; ms from the call's start).
+    kernel_busy_ms is the union of the chunks' kernel intervals, idle_ms the
+    rest of the call, and overlap_frac the share of the copy-only time that
+    the call hid behind its kernels: (kernel_busy + copy_only - wall) /
+    copy_only."""
+    wall = max(t[3] for t in tl)
+    spans = sorted((t[1], t[2]) for t in tl)
+    busy, cur_s, cur_e, gaps = 0.0, None, None, []
+    for s, e in spans:
+        if cur_e is None or s > cur_e:
+            if cur_e is not None:
+                busy += cur_e - cur_s
+                gaps.append(s - cur_e)
+            cur_s, cur_e = s, e
+        else:
+            cur_e = max(cur_e, e)
+    busy += cur_e - cur_s
+    kernel_sum = sum(t[2] - t[1] for t in tl)
+    waits_on_copy = sum(max(0.0, tl[c][0] - tl[c - 1][2]) for c in range(1, len(tl)))
+    return {"chunks": len(tl), "wall_ms": round(wall, 3), "kernel_busy_ms": round(busy, 3),
+            "kernel_ms_sum": round(kernel_sum, 3), "idle_ms": round(wall - busy, 3),
+            "first_kernel_ms": round(spans[0][0], 3), "after_last_kernel_ms": round(wall - cur_e, 3),
+            "max_gap_ms": round(max(gaps), 3) if gaps else 0.0,
+            "copy_in_late_ms": round(waits_on_copy, 3),
+            "overlap_frac": round(max(0.0, min(1.0, (busy + copy_only_ms - wall) / copy_only_ms)), 4)
+            if copy_only_ms > 0 else None}
 
 
 def _oracle_sample_rate(q_rows, k_head, v_head, scale, causal, positions, budget_s):
@@ -792,7 +858,7 @@ def main():
     ap.add_argument("--dec-len", type=int, default=DEC["S"], help="decode cached keys per sequence")
     ap.add_argument("--dec-splits", type=int, default=0, help="decode-one: split count (0: the heuristic's)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-seconds", type=float, default=8.0)
+    ap.add_argument("--ref-seconds", type=float, default=4.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.mode == "decode-sweep":

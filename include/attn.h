@@ -155,6 +155,29 @@ size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d,
                                      int kv_heads_per_chunk);
 
 /*
+ * Timeline of attn_fwd_host, for measuring how far its copies overlap its
+ * kernels (instrumentation; the pages define no such call).
+ * attn_fwd_host_trace(1) makes every later attn_fwd_host call on the current
+ * device record CUDA timing events: one on `stream` as the call starts and,
+ * per chunk, one after its copy-in, one when its compute stream reaches the
+ * kernel launch, one after the kernel and one after its copy-out.
+ * attn_fwd_host_trace(0) stops recording.  Returns ATTN_OK or ATTN_ERR_CUDA.
+ * Tracing adds only event records to the same streams; do not trace a call
+ * that is being captured into a CUDA graph.
+ *
+ * attn_fwd_host_trace_read waits for the last traced call on the current
+ * device to finish and writes, for chunk c < capacity, four times in
+ * milliseconds from the call's start into ms[4c .. 4c+3]: copy-in done,
+ * kernel reached, kernel done, copy-out done.  Chunks are numbered in the
+ * call's order (batch entry, then KV-head chunk).  Returns the call's chunk
+ * count (which may exceed capacity), ATTN_ERR_ARG if ms is NULL with
+ * capacity > 0 or no traced call has been made since tracing was switched
+ * on, or ATTN_ERR_CUDA.
+ */
+int attn_fwd_host_trace(int enable);
+long long attn_fwd_host_trace_read(float *ms, long long capacity);
+
+/*
  * Backward pass of attn_fwd: gradients dQ, dK, dV for the output gradient
  * dout.  The pages measure an FA2 backward pass under the same tile orders
  * (detail page, section 5 "backward pass"); the gradient itself is the chain
@@ -251,6 +274,11 @@ int attn_decode(const void *q, const void *kcache, const void *vcache, const int
  * Set-up: the first call on each device looks up the device address of the
  * scratch array (cudaGetSymbolAddress, with that device current) and keeps
  * it for later calls.  Make that first call before capturing any stream.
+ * The kept address belongs to the context that was current on that first
+ * call (normally the device's primary context, which the runtime API uses):
+ * after cudaDeviceReset, or from another driver context made current on the
+ * same device, the library's module is loaded anew and the kept address is
+ * stale, so do not call this entry point in either situation.
  *
  * Sharing: all calls use the same array, and it keeps whatever the last call
  * wrote.  Each call writes every partial it later reads, so nothing needs

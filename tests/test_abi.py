@@ -34,6 +34,22 @@ def test_every_declared_symbol_is_exported(L):
     assert names == set(attn.SIGNATURES), "binding and header disagree"
 
 
+def test_noalloc_scratch_size_agrees_with_the_header(L):
+    """The binding's copy of the built-in scratch size is the header's value
+    (the library itself checks the header against its own constant when it
+    compiles)."""
+    text = open(os.path.join(ROOT, "include", "attn.h")).read()
+    m = re.search(r"#define\s+ATTN_DECODE_NOALLOC_SCRATCH_BYTES\s+(\d+)u?", text)
+    assert m, "ATTN_DECODE_NOALLOC_SCRATCH_BYTES not found in attn.h"
+    assert int(m.group(1)) == attn.DECODE_NOALLOC_SCRATCH_BYTES
+
+
+def test_fwd_host_trace_read_checks_its_buffer(L):
+    # a capacity without a buffer is refused before any CUDA call
+    assert L.attn_fwd_host_trace_read(None, 4) == attn.ATTN_ERR_ARG
+    assert L.attn_fwd_host_trace_read(None, -1) == attn.ATTN_ERR_ARG
+
+
 def test_version_and_messages(L):
     assert attn.attn_version() >= 100
     for code in (0, -1, -2, -3, -4, -5):

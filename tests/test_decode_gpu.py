@@ -1,7 +1,7 @@
 """GPU parity of the split-KV decode and the log-sum-exp merge against the
 fp64 oracle, through the C ABI: ragged and empty sequences, several split
 counts (including empty splits), the workspace partials themselves, group
-sizes 1..16, and the full decode configurations on sampled (batch, head)."""
+sizes 1..16, and every element of the full decode configurations."""
 import gc
 
 import numpy as np
@@ -152,22 +152,42 @@ FULL = [(b, s) for b in (1, 8, 32) for s in (8192, 32768, 131072)]
 
 
 @pytest.mark.parametrize("B,S", FULL)
-def test_full_size_sampled(attn, B, S):
+def test_full_size_every_element(attn, B, S):
+    """The GQA decode configurations (Hq=64, Hkv=8, d=128, batch 1/8/32, KV
+    length 8K/32K/128K, the heuristic's split count), every output element
+    against the oracle.  The oracle runs on one (batch entry, KV head) pair's
+    slices at a time, so only that pair's cache is ever widened to fp64; the
+    pairs of one batch entry run on a thread pool (the oracle's C calls
+    release the interpreter lock)."""
+    from concurrent.futures import ThreadPoolExecutor
     dev = torch.device("cuda")
     Hq, Hkv, d = 64, 8, 128
+    G = Hq // Hkv
     q, kc, vc = decode_inputs(70, B, Hq, Hkv, S, d, dev)
-    lens = [S] * B
-    seqlens = torch.tensor(lens, dtype=torch.int32, device=dev)
+    seqlens = torch.full((B,), S, dtype=torch.int32, device=dev)
     try:
         o, _, used = attn.decode(q, kc, vc, seqlens, num_splits=0)
         torch.cuda.synchronize()
         attn.check(attn.attn_device_status(), "device status")
-        for b in sorted({0, B // 2, B - 1}):
-            for g in (0, Hkv - 1):
-                heads = list(range(g * (Hq // Hkv), (g + 1) * (Hq // Hkv)))
-                o_ref, _ = oracle.decode(to64(q[b:b + 1, heads]), to64(kc[b:b + 1, g:g + 1]),
-                                         to64(vc[b:b + 1, g:g + 1]), [S], scale_of(d))
-                assert_close(to64(o[b:b + 1, heads]), o_ref, what=f"B={B} S={S} b={b} g={g} splits={used}")
+        o64 = to64(o)
+        q64 = to64(q)
+
+        def pair(b, g, k64, v64):
+            o_ref, _ = oracle.decode(q64[b:b + 1, g * G:(g + 1) * G], k64[None, None], v64[None, None], [S],
+                                     scale_of(d))
+            return b, g, o_ref
+
+        with ThreadPoolExecutor(max_workers=min(Hkv, oracle.default_threads())) as pool:
+            for b in range(B):
+                # widen on the device, one batch entry at a time
+                kb = kc[b].double().cpu().numpy()
+                vb = vc[b].double().cpu().numpy()
+                jobs = [pool.submit(pair, b, g, kb[g], vb[g]) for g in range(Hkv)]
+                for j in jobs:
+                    bb, g, o_ref = j.result()
+                    assert_close(o64[bb:bb + 1, g * G:(g + 1) * G], o_ref,
+                                 what=f"B={B} S={S} b={bb} g={g} splits={used}")
+                del kb, vb
     finally:
         del q, kc, vc
         gc.collect()

@@ -126,3 +126,30 @@ def test_host_buffers_need_no_alignment(attn):
     attn.check(attn.attn_device_status(), "device status")
     assert torch.equal(o_h.view(torch.int16), o_dev.cpu().view(torch.int16))
     assert torch.equal(lse_h, lse_dev.cpu())
+
+
+def test_traced_call_records_an_ordered_timeline(attn):
+    """With tracing on, a call records per chunk (copy-in done, kernel
+    reached, kernel done, copy-out done); each chunk's times are ordered that
+    way, the chunks follow the call's chunk order, and the traced call's
+    outputs are those of an untraced one."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N, d = 2, 8, 4, 700, 128
+    q, k, v = prefill_inputs(4, B, Hq, Hkv, N, d, dev)
+    hq, hk, hv = (_host(t, True) for t in (q, k, v))
+    o0, lse0 = attn.forward_host(hq, hk, hv, kv_heads_per_chunk=1)
+    with pytest.raises(attn.AttnError):
+        attn.attn_fwd_host_trace_read()  # nothing traced yet
+    attn.check(attn.attn_fwd_host_trace(1), "trace on")
+    try:
+        o1, lse1 = attn.forward_host(hq, hk, hv, kv_heads_per_chunk=1)
+        tl = attn.attn_fwd_host_trace_read()
+    finally:
+        attn.check(attn.attn_fwd_host_trace(0), "trace off")
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16)) and torch.equal(lse0, lse1)
+    assert len(tl) == B * Hkv
+    for c, (cin, kin, kout, cout) in enumerate(tl):
+        assert 0.0 <= cin <= kin <= kout <= cout, (c, tl[c])
+        if c >= 2:  # a slot is refilled only after the chunk two back has left it
+            assert cin >= tl[c - 2][2] - 1e-3, (c, tl[c], tl[c - 2])
+    assert len(attn.attn_fwd_host_trace_read(capacity=3)) == 3

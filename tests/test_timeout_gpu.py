@@ -22,7 +22,8 @@ def attn():
     return A
 
 
-# d = 64 runs the half-row softmax, whose paired warps agree on every give-up.
+# Both forward instantiations (d <= 64 and d = 128): every role of a CTA leaves
+# its loop once one wait gives up, and the next launch runs normally.
 @pytest.mark.parametrize("d", [64, 128])
 def test_forward_timeout_is_reported_and_recovered(attn, d):
     dev = torch.device("cuda")
