@@ -225,7 +225,7 @@ int fwd_host_trace(int enable) {
     if (dev < 0 || dev >= kMaxDevices) return note_cuda_error(cudaErrorInvalidDevice, "device index");
     std::lock_guard<std::mutex> lock(g_pipe_mu);
     g_trace[dev].on = enable != 0;
-    g_trace[dev].valid = false;
+    if (enable) g_trace[dev].valid = false;  // switching off keeps the last timeline readable
     return 0;
 }
 

@@ -161,7 +161,8 @@ size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d,
  * device record CUDA timing events: one on `stream` as the call starts and,
  * per chunk, one after its copy-in, one when its compute stream reaches the
  * kernel launch, one after the kernel and one after its copy-out.
- * attn_fwd_host_trace(0) stops recording.  Returns ATTN_OK or ATTN_ERR_CUDA.
+ * attn_fwd_host_trace(0) stops recording (the last timeline stays readable).
+ * Returns ATTN_OK or ATTN_ERR_CUDA.
  * Tracing adds only event records to the same streams; do not trace a call
  * that is being captured into a CUDA graph.
  *
