@@ -29,6 +29,10 @@ ORDER_DIE_SPLIT_HEAD_FIRST = 3
 ORDERS = {"head_first": ORDER_HEAD_FIRST, "block_first": ORDER_BLOCK_FIRST,
           "naive_head_first": ORDER_NAIVE_HEAD_FIRST,
           "die_split_head_first": ORDER_DIE_SPLIT_HEAD_FIRST}
+# forward tile schemes, OR-ed into tile_order (0: the library's choice)
+FWD_SINGLE_CTA = 0x100
+FWD_CTA_PAIR = 0x200
+SCHEMES = {"auto": 0, "single": FWD_SINGLE_CTA, "pair": FWD_CTA_PAIR}
 
 # Every symbol include/attn.h declares, with (restype, argtypes).
 _P = ctypes.c_void_p

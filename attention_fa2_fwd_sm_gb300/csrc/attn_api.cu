@@ -82,6 +82,12 @@ bool encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t dim0, uint64_t 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int fwd_run(const FwdLaunch &a, cudaStream_t stream) {
+    // The library's choice: the one-CTA kernel (every head dimension).
+    if (a.scheme == kSchemePair) return fwd_pair_launch(a, stream);
+    return fwd_launch(a, stream);
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -161,12 +167,25 @@ int attn_die_map(int *die_of_sm, int capacity, float *stats) {
     return die_map_query(die_of_sm, capacity, stats);
 }
 
+// tile_order of the forward entry points: an order in the low byte, at most
+// one tile-scheme flag above it.
+static int order_of(int tile_order) { return tile_order & 0xff; }
+static int scheme_of(int tile_order) {
+    const int f = tile_order & ~0xff;
+    if (f == 0) return kSchemeAuto;
+    if (f == ATTN_FWD_SINGLE_CTA) return kSchemeSingle;
+    if (f == ATTN_FWD_CTA_PAIR) return kSchemePair;
+    return -1;
+}
+
 static int validate_fwd_sizes(int B, int Hq, int Hkv, int N, int d, float scale, int tile_order) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0) return ATTN_ERR_ARG;
     if (Hq % Hkv) return ATTN_ERR_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_ARG;
-    if (tile_order < kHeadFirst || tile_order > kDieSplitHeadFirst) return ATTN_ERR_ARG;
+    const int order = order_of(tile_order), scheme = scheme_of(tile_order);
+    if (order < kHeadFirst || order > kDieSplitHeadFirst || scheme < 0) return ATTN_ERR_ARG;
     if (d != 56 && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (scheme == kSchemePair && d != 128) return ATTN_ERR_UNSUPPORTED;
     // tensor-map limits: each dimension < 2^32, strides < 2^40 bytes
     if ((long long)B * Hq >= (1LL << 31) || (long long)N * d * 2 >= (1LL << 39)) return ATTN_ERR_ARG;
     // The persistent forward and backward kernels take work units (at most
@@ -195,7 +214,8 @@ static FwdLaunch fwd_problem(int B, int Hq, int Hkv, int N, int d, float scale, 
     a.d = d;
     a.scale = scale;
     a.causal = causal ? 1 : 0;
-    a.order = tile_order;
+    a.order = order_of(tile_order);
+    a.scheme = scheme_of(tile_order);
     a.wait_ns = (unsigned long long)g_wait_ns.load();
     a.num_sms = sms;
     return a;
@@ -214,7 +234,7 @@ int attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse
     a.v = v;
     a.o = o;
     a.lse = lse;
-    return fwd_launch(a, reinterpret_cast<cudaStream_t>(stream));
+    return fwd_run(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int kv_heads_per_chunk) {
@@ -492,11 +512,11 @@ int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, c
 int attn_device_status(attn_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    int a = 0, b = 0, c = 0;
+    int a = 0, b = 0, c = 0, e = 0;
     if (fwd_take_status(&a) != cudaSuccess || decode_take_status(&b) != cudaSuccess ||
-        bwd_take_status(&c) != cudaSuccess)
+        bwd_take_status(&c) != cudaSuccess || fwd_pair_take_status(&e) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    return (a | b | c) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    return (a | b | c | e) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 }  // extern "C"

@@ -9,6 +9,10 @@
 
 namespace attn {
 
+// Forward tile schemes: one 256-row unit per SM, or 512-row units on CTA
+// pairs (cta_group::2 MMAs).
+enum FwdScheme : int { kSchemeAuto = 0, kSchemeSingle = 1, kSchemePair = 2 };
+
 struct FwdLaunch {
     const void *q, *k, *v;
     void *o;
@@ -18,6 +22,7 @@ struct FwdLaunch {
     int causal, order;
     unsigned long long wait_ns;
     int num_sms;
+    int scheme = kSchemeAuto;
 };
 
 struct BwdLaunch {
@@ -91,7 +96,12 @@ inline int slot_for_device() {
 int note_cuda_error(cudaError_t e, const char *where);
 
 // Each returns 0 or a negative ATTN_ERR_* code.
+// fwd_run picks the launcher for a.scheme (fwd_launch: one CTA per unit;
+// fwd_pair_launch: CTA pairs, d = 128 only).
+int fwd_run(const FwdLaunch &a, cudaStream_t stream);
 int fwd_launch(const FwdLaunch &a, cudaStream_t stream);
+int fwd_pair_launch(const FwdLaunch &a, cudaStream_t stream);
+int fwd_pair_units_per_head(int N);
 int decode_launch(const DecodeLaunch &a, cudaStream_t stream);
 int bwd_launch(const BwdLaunch &a, cudaStream_t stream);
 
@@ -117,6 +127,7 @@ int die_map_query(int *die_of_sm, int capacity, float *stats);
 // Read and clear the status word of each kernel translation unit (OR of
 // kStatus* bits).
 cudaError_t fwd_take_status(int *bits);
+cudaError_t fwd_pair_take_status(int *bits);
 cudaError_t decode_take_status(int *bits);
 cudaError_t bwd_take_status(int *bits);
 

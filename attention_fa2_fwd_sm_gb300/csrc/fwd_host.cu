@@ -191,7 +191,7 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
         f.Hq = hn;
         f.Hkv = gn;
         ATTN_CK(trace_mark(c, 1, cs), "cudaEventRecord (trace)");
-        const int rc = fwd_launch(f, cs);
+        const int rc = fwd_run(f, cs);
         if (rc != 0) {
             join_internal();
             return rc;

@@ -46,16 +46,16 @@ DEC = dict(B=32, Hq=64, Hkv=8, S=131072, d=128)
 # bench reports null until re-captured.
 MEASURED_TRAFFIC = {
     "fwd": {"files": ["fwd_sm103.cu", "sm103_ptx.cuh", "tile_order.cuh"],
-            "sha256": None,
+            "sha256": "6941f2c90f2f9fd297d4fa680bd15435239464c3eb0d1a5bbb847666e984ee3b",
             # MHA B=1 d=128 non-causal, head-first, H = Hq = Hkv = 16 at N = 131072
             # (one-pass capture of dram__bytes_read.sum + dram__bytes_write.sum)
             "capture": {"B": 1, "H": 16, "N": 131072, "d": 128, "causal": False,
-                        "order": "head_first", "bytes": None}},
+                        "order": "head_first", "bytes": 5070208000 + 606743296}},
     "decode": {"files": ["decode_sm103.cu", "sm103_ptx.cuh"],
-               "sha256": None,
+               "sha256": "eea28fbd34c4bacf564487ff290b51fa5037287fc8703873f7b0f1aabac57512",
                # GQA decode Hq=64 Hkv=8 d=128, B=4 sequences of 131072 keys, 2 splits
                # (the heuristic's count at B=32), decode kernel only
-               "capture": {"B": 4, "S": 131072, "splits": 2, "bytes": None}},
+               "capture": {"B": 4, "S": 131072, "splits": 2, "bytes": 2147677696 + 2685696}},
 }
 
 
@@ -606,6 +606,17 @@ def run_fwd_sweep(args):
                           "frac": round(tf / peaks["bf16_tflops"], 4)}
             if d == 56:
                 out[oname]["tflops_padded_d64"] = round(tf * 64 / 56, 1)
+        if d == 128:
+            # the CTA-pair scheme (cta_group::2) in the head-first and block-first orders
+            for oname in ("head_first", "block_first"):
+                oid = attn.ORDERS[oname] | attn.FWD_CTA_PAIR
+                fn = lambda: attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, d ** -0.5, causal,
+                                                         oid, stream.cuda_stream), "fwd pair")
+                fn()
+                ms = _time_calls(torch, fn, reps, None, stream)
+                tf = flops / (ms / 1e3) / 1e12
+                out["pair_" + oname] = {"ms": round(ms, 3), "tflops": round(tf, 1),
+                                        "frac": round(tf / peaks["bf16_tflops"], 4)}
         print(json.dumps(out), flush=True)
         del q, k, v, o, lse
         torch.cuda.empty_cache()
@@ -629,7 +640,7 @@ def run_fwd_one(args):
     q, k, v = prefill_inputs(12, B, Hq, Hkv, N, d, dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-    oid = attn.ORDERS[args.order]
+    oid = attn.ORDERS[args.order] | attn.SCHEMES[args.scheme]
     fn = lambda: attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, d ** -0.5, causal, oid,
                                              stream.cuda_stream), "fwd")
     for _ in range(args.warmup):
@@ -638,7 +649,7 @@ def run_fwd_one(args):
     flops = fwd_flops(B, Hq, N, d, causal)
     tf = flops / (ms / 1e3) / 1e12
     print(json.dumps({"mode": "fwd-one", "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": causal,
-                      "order": args.order, "ms": round(ms, 4), "tflops": round(tf, 1),
+                      "order": args.order, "scheme": args.scheme, "ms": round(ms, 4), "tflops": round(tf, 1),
                       "frac": round(tf / peaks["bf16_tflops"], 4), "launches": args.warmup + args.steps}),
           flush=True)
 
@@ -851,6 +862,8 @@ def main():
     ap.add_argument("--order", default="head_first", choices=["head_first", "block_first",
                                                               "naive_head_first",
                                                               "die_split_head_first"])
+    ap.add_argument("--scheme", default="auto", choices=["auto", "single", "pair"],
+                    help="fwd-one: forward tile scheme (pair: CTA pairs with cta_group::2 MMAs, d = 128)")
     ap.add_argument("--no-ablation", dest="ablation", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")

@@ -90,6 +90,23 @@ enum attn_tile_order {
     ATTN_ORDER_DIE_SPLIT_HEAD_FIRST = 3
 };
 
+/* Tile schemes of the forward kernel, OR-ed into the tile_order argument of
+ * attn_fwd_ex and attn_fwd_host (at most one):
+ *  ATTN_FWD_SINGLE_CTA: each SM runs units of 256 query rows (two 128-row
+ *    MMA tiles sharing every K/V block it loads).
+ *  ATTN_FWD_CTA_PAIR: pairs of SMs (a cluster of two CTAs) run units of 512
+ *    query rows with tcgen05 MMAs of the cta_group::2 kind (M = 256): each SM
+ *    loads half of every K/V block and one thread issues the MMAs of both.
+ *    The pages keep the workgroups that share one head's K/V on one chiplet
+ *    (detail page, section 2 Q1-Q2); a pair shares each block through the
+ *    MMA itself.  d = 128 only (ATTN_ERR_UNSUPPORTED otherwise).  The units
+ *    of the orders above are then 512-row blocks.
+ * Without a flag the library picks the scheme.  Results agree across
+ * schemes within the forward's tolerance; every order of one scheme gives
+ * bit-identical results. */
+#define ATTN_FWD_SINGLE_CTA 0x100
+#define ATTN_FWD_CTA_PAIR 0x200
+
 /*
  * Forward (prefill) attention.  Detail page, section 4 equation; FA2 tiling of
  * Figure 4 (each CTA owns a block of query rows and streams all of K and V).

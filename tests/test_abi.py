@@ -303,3 +303,17 @@ def test_host_forward_workspace_size(L):
     assert attn.attn_fwd_host_workspace_bytes(1, 64, 8, 512, 128, 0) == 2 * slot(8, 8, 512, 128)
     assert attn.attn_fwd_host_workspace_bytes(1, 4, 2, 100, 64, 3) == 0
     assert attn.attn_fwd_host_workspace_bytes(1, 4, 2, 100, 32, 1) == 0
+
+
+def test_forward_tile_scheme_flags_are_validated(L):
+    """The scheme flags ride in tile_order; the pair scheme is d = 128 only.
+    All refused on the host, before any CUDA call."""
+    args = lambda order, d: (A16, A16, A16, A16, None, 1, 2, 2, 256, d, 0.125, 0, order, 0)
+    assert attn.attn_fwd_ex(*args(attn.FWD_CTA_PAIR, 64)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_fwd_ex(*args(attn.FWD_CTA_PAIR | 1, 56)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_fwd_ex(*args(attn.FWD_CTA_PAIR | attn.FWD_SINGLE_CTA, 128)) == attn.ATTN_ERR_ARG
+    assert attn.attn_fwd_ex(*args(0x400, 128)) == attn.ATTN_ERR_ARG
+    assert attn.attn_fwd_ex(*args(attn.FWD_CTA_PAIR | 4, 128)) == attn.ATTN_ERR_ARG
+    assert attn.attn_fwd_ex(*args(-1, 128)) == attn.ATTN_ERR_ARG
+    # the backward pass takes plain orders only
+    assert _bwd(order=attn.FWD_SINGLE_CTA, d=128) == attn.ATTN_ERR_ARG
