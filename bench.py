@@ -731,6 +731,47 @@ def run_decode_one(args):
                       "l2": "flushed before every call"}), flush=True)
 
 
+def run_decode_floor(args):
+    """What bounds the short decode configurations: each (B, S) timed as is,
+    with every sequence empty (the same grid and merge, no keys to read),
+    with 64 keys per sequence (one ring stage per CTA that has keys), and the
+    same three with one split (one kernel, no merge).  The L2 is flushed
+    before every call; one JSON line per configuration."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import decode_inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    flush = _l2_flush_buffer(torch, dev)
+    stream = torch.cuda.current_stream(dev)
+    Hq, Hkv, d = DEC["Hq"], DEC["Hkv"], DEC["d"]
+    for B, S in ((1, 8192), (1, 32768), (8, 8192), (8, 32768)):
+        q, kc, vc = decode_inputs(70, B, Hq, Hkv, S, d, dev)
+        o = torch.empty_like(q)
+        heur = attn.attn_decode_num_splits(B, Hq, Hkv, S)
+        out = {"mode": "decode-floor", "B": B, "S": S, "heuristic_splits": heur,
+               "bytes": 2 * B * Hkv * S * d * 2 + 2 * B * Hq * d * 2}
+        for sp in (heur, 1):
+            wb = attn.attn_decode_workspace_bytes(B, Hq, d, sp)
+            ws = torch.empty(max(wb, 16), dtype=torch.uint8, device=dev)
+            for name, n in (("full", S), ("one_stage", 64), ("empty", 0)):
+                seq = torch.full((B,), n, dtype=torch.int32, device=dev)
+                fn = lambda: attn.check(attn.attn_decode(q, kc, vc, seq, o, B, Hq, Hkv, d, d ** -0.5, sp, S, ws, wb,
+                                                         stream.cuda_stream), "decode")
+                for _ in range(args.warmup):
+                    fn()
+                out[f"{name}_splits{sp}_us"] = round(_time_calls(torch, fn, args.steps, flush, stream) * 1e3, 2)
+        out["full_gbs"] = round(out["bytes"] / (out[f"full_splits{heur}_us"] * 1e-6) / 1e9, 1)
+        out["frac_hbm"] = round(out["full_gbs"] / peaks["hbm_gbs"], 4)
+        print(json.dumps(out), flush=True)
+        del q, kc, vc
+        torch.cuda.empty_cache()
+
+
 def run_decode_varlen(args):
     """Ragged multi-user decode batches (GQA Hq=64, Hkv=8, d=128): attn_decode
     (split count from max_seqlen) against attn_decode_varlen (chunks from the
@@ -849,7 +890,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--mode", default="step",
-                    choices=["step", "decode-sweep", "decode-one", "decode-varlen", "fwd-sweep", "fwd-one",
+                    choices=["step", "decode-sweep", "decode-one", "decode-floor", "decode-varlen", "fwd-sweep", "fwd-one",
                              "bwd-one", "bwd-sweep", "die-map"],
                     help="step: the contract's one-line benchmark; the sweeps print one line "
                          "per configuration; fwd-one times one forward configuration")
@@ -888,6 +929,8 @@ def main():
         return run_decode_one(args)
     if args.mode == "decode-varlen":
         return run_decode_varlen(args)
+    if args.mode == "decode-floor":
+        return run_decode_floor(args)
     if args.mode == "bwd-sweep":
         return run_bwd_sweep(args)
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
