@@ -47,6 +47,8 @@ SIGNATURES = {
     "attn_fwd_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _I, _P, _SZ, _P]),
     "attn_fwd_host_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "attn_fwd_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
+    "attn_fwd_splitkv_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "attn_fwd_host_trace": (_I, [_I]),
     "attn_fwd_host_trace_read": (_LL, [_FP, _LL]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
@@ -142,6 +144,36 @@ def attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, tile_order, 
 
 def attn_fwd_host_workspace_bytes(B, Hq, Hkv, N, d, kv_heads_per_chunk=0) -> int:
     return int(lib().attn_fwd_host_workspace_bytes(B, Hq, Hkv, N, d, kv_heads_per_chunk))
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, kv_splits, workspace, workspace_bytes,
+                     stream=None) -> int:
+    return lib().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
+                                  int(bool(causal)), int(kv_splits), _ptr(workspace), int(workspace_bytes),
+                                  _stream(stream))
+
+
+def attn_fwd_splitkv_workspace_bytes(B, Hq, N, d, kv_splits=0) -> int:
+    return int(lib().attn_fwd_splitkv_workspace_bytes(B, Hq, N, d, kv_splits))
+
+
+def forward_splitkv(q, k, v, causal=False, scale=None, kv_splits=0, workspace=None, with_lse=True, stream=None):
+    """Allocate outputs (and a workspace when none is given) and run
+    attn_fwd_splitkv on ``[B, H, N, d]`` bf16 CUDA tensors; returns
+    ``(o, lse, workspace)``."""
+    import torch
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    nbytes = attn_fwd_splitkv_workspace_bytes(B, Hq, N, d, kv_splits)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if with_lse else None
+    check(attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, kv_splits, workspace, nbytes,
+                           stream), "attn_fwd_splitkv")
+    return o, lse, workspace
 
 
 def attn_fwd_host_trace(enable) -> int:

@@ -277,6 +277,76 @@ long long attn_fwd_host_trace_read(float *ms, long long capacity) {
     return n == -1 ? ATTN_ERR_ARG : n;
 }
 
+// Split-KV forward: the key range of each head in `splits` pieces of
+// `chunk_keys` keys (a multiple of the 128-key block); kv_splits <= 0 picks
+// the fewest pieces whose K and V of one KV head fit in 32 MiB.
+constexpr int kMaxKvSplits = 64;
+static bool splitkv_plan(int N, int d, int kv_splits, int *splits, int *chunk_keys) {
+    if (kv_splits > kMaxKvSplits) return false;
+    int s = kv_splits;
+    if (s <= 0) {
+        const long long budget_keys = (32LL << 20) / (4LL * d);  // K + V bf16 of one head per key: 4 d bytes
+        s = int((N + budget_keys - 1) / budget_keys);
+        if (s < 1) s = 1;
+        if (s > kMaxKvSplits) s = kMaxKvSplits;
+    }
+    long long chunk = (N + s - 1) / s;
+    chunk = (chunk + 127) / 128 * 128;
+    *chunk_keys = int(chunk);
+    *splits = int((N + chunk - 1) / chunk);
+    return true;
+}
+
+static void splitkv_layout(int B, int Hq, int N, int d, int splits, size_t *o_bytes, size_t *lse_bytes) {
+    const size_t rows = (size_t)B * Hq * N;
+    *o_bytes = (rows * splits * d * sizeof(float) + 255) / 256 * 256;
+    *lse_bytes = rows * splits * sizeof(float);
+}
+
+size_t attn_fwd_splitkv_workspace_bytes(int B, int Hq, int N, int d, int kv_splits) {
+    if (B <= 0 || Hq <= 0 || N <= 0 || (d != 56 && d != 64 && d != 128)) return 0;
+    int splits = 0, chunk = 0;
+    if (!splitkv_plan(N, d, kv_splits, &splits, &chunk)) return 0;
+    size_t a = 0, b = 0;
+    splitkv_layout(B, Hq, N, d, splits, &a, &b);
+    return a + b;
+}
+
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
+                     int N, int d, float scale, int causal, int kv_splits, void *workspace, size_t workspace_bytes,
+                     attn_stream_t stream) {
+    int rc = validate_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, kHeadFirst);
+    if (rc != ATTN_OK) return rc;
+    int splits = 0, chunk = 0;
+    if (!splitkv_plan(N, d, kv_splits, &splits, &chunk)) return ATTN_ERR_ARG;
+    if ((long long)B * Hq * unit_blocks(N) * splits >= (1LL << 31)) return ATTN_ERR_ARG;
+    size_t o_bytes = 0, lse_bytes = 0;
+    splitkv_layout(B, Hq, N, d, splits, &o_bytes, &lse_bytes);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < o_bytes + lse_bytes) return ATTN_ERR_WORKSPACE;
+    const int sms = current_num_sms();
+    if (sms <= 0) return note_cuda_error(cudaErrorNoDevice, "device query");
+    FwdSplitLaunch a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.splits = splits;
+    a.chunk_keys = chunk;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
+    a.wait_ns = (unsigned long long)g_wait_ns.load();
+    a.num_sms = sms;
+    return fwd_split_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
              int Hkv, int N, int d, float scale, int causal, attn_stream_t stream) {
     return attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, ATTN_ORDER_HEAD_FIRST,
@@ -512,11 +582,12 @@ int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, c
 int attn_device_status(attn_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    int a = 0, b = 0, c = 0, e = 0;
+    int a = 0, b = 0, c = 0, e = 0, f = 0;
     if (fwd_take_status(&a) != cudaSuccess || decode_take_status(&b) != cudaSuccess ||
-        bwd_take_status(&c) != cudaSuccess || fwd_pair_take_status(&e) != cudaSuccess)
+        bwd_take_status(&c) != cudaSuccess || fwd_pair_take_status(&e) != cudaSuccess ||
+        fwd_split_take_status(&f) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    return (a | b | c | e) ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    return (a | b | c | e | f) ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
 }  // extern "C"

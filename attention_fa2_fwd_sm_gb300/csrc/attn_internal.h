@@ -102,6 +102,24 @@ int fwd_run(const FwdLaunch &a, cudaStream_t stream);
 int fwd_launch(const FwdLaunch &a, cudaStream_t stream);
 int fwd_pair_launch(const FwdLaunch &a, cudaStream_t stream);
 int fwd_pair_units_per_head(int N);
+
+// Split-KV forward (fwd_splitkv_sm103.cu): `fwd`'s problem with every head's
+// keys cut into `splits` ranges of `chunk_keys` keys (a multiple of 128); the
+// partials go to part_o ([splits][B * Hq][N][d] fp32) and part_lse
+// ([splits][B * Hq][N] fp32), then a merge kernel writes o and lse.
+struct FwdSplitLaunch {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    int B, Hq, Hkv, N, d;
+    float scale;
+    int causal;
+    int splits, chunk_keys;
+    float *part_o, *part_lse;
+    unsigned long long wait_ns;
+    int num_sms;
+};
+int fwd_split_launch(const FwdSplitLaunch &a, cudaStream_t stream);
 int decode_launch(const DecodeLaunch &a, cudaStream_t stream);
 int bwd_launch(const BwdLaunch &a, cudaStream_t stream);
 
@@ -128,6 +146,7 @@ int die_map_query(int *die_of_sm, int capacity, float *stats);
 // kStatus* bits).
 cudaError_t fwd_take_status(int *bits);
 cudaError_t fwd_pair_take_status(int *bits);
+cudaError_t fwd_split_take_status(int *bits);
 cudaError_t decode_take_status(int *bits);
 cudaError_t bwd_take_status(int *bits);
 

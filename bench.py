@@ -654,6 +654,54 @@ def run_fwd_one(args):
           flush=True)
 
 
+def run_fwd_splitkv(args):
+    """The sub-ACC split (attn_fwd_splitkv) against the plain head-first
+    forward on the long configurations: MHA and causal GQA at N = 131072
+    (d = 128) and the DeepSeek-like d = 56 causal one; W warm-up calls, then
+    K timed calls (median).  One JSON line per configuration."""
+    import torch
+
+    import attention_fa2_fwd_sm_gb300 as attn
+    from attention_fa2_fwd_sm_gb300 import _build
+    from synthetic_inputs import prefill_inputs
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, _ = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    configs = [("mha", 1, 128, 128, 131072, 128, False), ("gqa", 1, 64, 8, 131072, 128, True),
+               ("deepseek", 1, 128, 128, 131072, 56, True)]
+    if args.hq != FWD["H"] or args.n != FWD["N"]:  # one configuration from the flags
+        configs = [("one", args.batch, args.hq, args.hkv, args.n, args.head_dim, args.causal)]
+    for name, B, Hq, Hkv, N, d, causal in configs:
+        q, k, v = prefill_inputs(12, B, Hq, Hkv, N, d, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+        flops = fwd_flops(B, Hq, N, d, causal)
+        out = {"mode": "fwd-splitkv", "config": name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": causal}
+        fn = lambda: attn.check(attn.attn_fwd_ex(q, k, v, o, lse, B, Hq, Hkv, N, d, d ** -0.5, causal, 0,
+                                                 stream.cuda_stream), "fwd")
+        for _ in range(args.warmup):
+            fn()
+        ms = _time_calls(torch, fn, args.steps, None, stream)
+        out["plain"] = {"ms": round(ms, 3), "tflops": round(flops / (ms / 1e3) / 1e12, 1)}
+        for sp in (0, 1, 2, 4, 8):
+            wb = attn.attn_fwd_splitkv_workspace_bytes(B, Hq, N, d, sp)
+            ws = torch.empty(wb, dtype=torch.uint8, device=dev)
+            fn = lambda: attn.check(attn.attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, N, d, d ** -0.5, causal, sp,
+                                                          ws, wb, stream.cuda_stream), "splitkv")
+            for _ in range(args.warmup):
+                fn()
+            ms = _time_calls(torch, fn, args.steps, None, stream)
+            out[f"splits{sp}"] = {"ms": round(ms, 3), "tflops": round(flops / (ms / 1e3) / 1e12, 1),
+                                  "workspace_gb": round(wb / 1e9, 2)}
+            del ws
+            torch.cuda.empty_cache()
+        print(json.dumps(out), flush=True)
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+
+
 def bwd_flops(B, H, N, d, causal):
     """Algorithmic backward work: five products of 2*N*N*d per head (dV, dP,
     dK, dQ and the recomputed S), half of that causal."""
@@ -891,6 +939,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--mode", default="step",
                     choices=["step", "decode-sweep", "decode-one", "decode-floor", "decode-varlen", "fwd-sweep", "fwd-one",
+                             "fwd-splitkv",
                              "bwd-one", "bwd-sweep", "die-map"],
                     help="step: the contract's one-line benchmark; the sweeps print one line "
                          "per configuration; fwd-one times one forward configuration")
@@ -931,6 +980,8 @@ def main():
         return run_decode_varlen(args)
     if args.mode == "decode-floor":
         return run_decode_floor(args)
+    if args.mode == "fwd-splitkv":
+        return run_fwd_splitkv(args)
     if args.mode == "bwd-sweep":
         return run_bwd_sweep(args)
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)

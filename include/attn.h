@@ -172,6 +172,38 @@ size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d,
                                      int kv_heads_per_chunk);
 
 /*
+ * Forward attention with each head's keys split into ranges (the "sub-ACC"
+ * split).  "Optimizing Attention on GPUs by Exploiting GPU Architectural NUMA
+ * Effects" (related-work page) suggests, for long contexts whose per-head K/V
+ * outgrows an L2 slice, splitting an Attention Compute Cluster's keys so that
+ * the workgroups running together stream a piece that fits.  Here the units
+ * of an ACC (the query heads of one KV head) run key range 0 for all their
+ * row blocks, then range 1, and so on; each writes fp32 partials (O_s
+ * normalised by its own sum, lse_s) to the workspace, and a merge kernel on
+ * the same stream combines every row's ranges with the log-sum-exp weights
+ * (kernbench2 "Fused Grouped-Query Attention", Case 4's (m, l, O) reduction).
+ * Same tensors, layouts, arguments and errors as attn_fwd (head-first order;
+ * d in {56, 64, 128}); the result agrees with attn_fwd within the forward's
+ * tolerance, not bit for bit (the merge reassociates the sums).
+ *   kv_splits   1..64 ranges; each range is ceil(N / kv_splits) keys rounded
+ *               up to 128 (so fewer ranges may result), or <= 0 for the
+ *               library's choice: the fewest ranges whose K and V of one KV
+ *               head fit in 32 MiB (one range up to N = 65536 at d = 128).
+ *   workspace   DEVICE memory, 16-byte aligned, of at least
+ *               attn_fwd_splitkv_workspace_bytes(B, Hq, N, d, kv_splits)
+ *               bytes: ranges x B x Hq x N x (d + 1) floats, rounded;
+ *               ATTN_ERR_WORKSPACE if missing or short.
+ * Two kernels run on `stream`.
+ */
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     int kv_splits, void *workspace, size_t workspace_bytes,
+                     attn_stream_t stream);
+
+/* Workspace bytes attn_fwd_splitkv needs (0 for invalid sizes). */
+size_t attn_fwd_splitkv_workspace_bytes(int B, int Hq, int N, int d, int kv_splits);
+
+/*
  * Timeline of attn_fwd_host, for measuring how far its copies overlap its
  * kernels (instrumentation; the pages define no such call).
  * attn_fwd_host_trace(1) makes every later attn_fwd_host call on the current

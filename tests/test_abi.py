@@ -317,3 +317,27 @@ def test_forward_tile_scheme_flags_are_validated(L):
     assert attn.attn_fwd_ex(*args(-1, 128)) == attn.ATTN_ERR_ARG
     # the backward pass takes plain orders only
     assert _bwd(order=attn.FWD_SINGLE_CTA, d=128) == attn.ATTN_ERR_ARG
+
+
+def test_splitkv_workspace_and_argument_errors(L):
+    # N = 1000, 3 ranges: ceil(1000 / 3) = 334 keys, rounded up to 384 -> 3 ranges
+    rows = 1 * 2 * 1000
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 2, 1000, 64, 3) == rows * 3 * 64 * 4 + rows * 3 * 4
+    # 4 ranges asked of 300 keys: 128-key ranges -> 3 ranges
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 1, 300, 128, 4) == 300 * 3 * 128 * 4 + 300 * 3 * 4
+    # the library's choice: K + V of one head in 32 MiB -> 65536 keys at d = 128
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 1, 65536, 128, 0) == 65536 * 128 * 4 + 65536 * 4
+    two = 131072 * 2
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 1, 131072, 128, 0) == two * 128 * 4 + two * 4
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 1, 1000, 128, 65) == 0
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 1, 1000, 32, 2) == 0
+    args = lambda **kw: dict(dict(q=A16, k=A16, v=A16, o=A16, lse=None, B=1, Hq=2, Hkv=2, N=256, d=64, scale=0.125,
+                                  causal=0, s=2, ws=A16, wb=1 << 30), **kw)
+    call = lambda a: attn.attn_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"],
+                                          a["d"], a["scale"], a["causal"], a["s"], a["ws"], a["wb"], 0)
+    assert call(args(s=65)) == attn.ATTN_ERR_ARG
+    assert call(args(q=None)) == attn.ATTN_ERR_ARG
+    assert call(args(Hq=3)) == attn.ATTN_ERR_ARG
+    assert call(args(d=32)) == attn.ATTN_ERR_UNSUPPORTED
+    assert call(args(ws=None)) == attn.ATTN_ERR_WORKSPACE
+    assert call(args(wb=100)) == attn.ATTN_ERR_WORKSPACE

@@ -217,3 +217,29 @@ def test_thread_count_does_not_change_results(oracle):
     a = oracle.attention_head(q, k, v, 0.3, True, qpos=np.arange(17, 50), nthreads=1)
     b = oracle.attention_head(q, k, v, 0.3, True, qpos=np.arange(17, 50), nthreads=5)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_key_range_partials_merge_to_the_full_causal_attention(oracle):
+    """Causal prefill over key ranges: each range's partial (O over the range,
+    normalised by its own sum, and its lse) merged with the log-sum-exp
+    weights gives the full attention; a row takes only the ranges that start
+    at or before it (the later ones attend no key).  The same identity as the
+    decode merge, for query rows at every position of a causal prefill."""
+    rng = np.random.default_rng(21)
+    N, d, C = 37, 8, 10  # ranges [0,10) [10,20) [20,30) [30,37)
+    q, k, v = (rng.standard_normal((N, d)) for _ in range(3))
+    scale = 0.4
+    o_full, lse_full = oracle.attention_head(q, k, v, scale, True)
+    starts = list(range(0, N, C))
+    parts_o = np.zeros((N, len(starts), d))
+    parts_l = np.full((N, len(starts)), -np.inf)
+    for s, lo in enumerate(starts):
+        o_s, l_s = oracle.attention_head(q, k, v, scale, True, k_lo=lo, k_hi=min(lo + C, N))
+        for i in range(N):
+            if lo <= i:  # the range holds at least key lo <= i
+                parts_o[i, s], parts_l[i, s] = o_s[i], l_s[i]
+            else:
+                assert l_s[i] == -np.inf  # no key of the range is attended
+    o_m, l_m = oracle.lse_merge(parts_o, parts_l)
+    assert np.abs(o_m - o_full).max() < 1e-12
+    assert np.abs(l_m - lse_full).max() < 1e-12
