@@ -349,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(C::kBarUQEmpty + qs));
                 if (u < 0) break;
                 const UnitWork w = unit_work(p, u);
+                // A causal unit whose rows all lie before its key range has no
+                // block to visit (the producer loads nothing for it).
+                if (w.nmax == 0) continue;
                 const long long f0 = fills;  // K_j at f0 + 2j, V_j at f0 + 2j + 1
                 // prologue: S(t, 0) = Q(t) K_0^T
                 ok = wait_slot(f0);
