@@ -813,6 +813,12 @@ def run_decode_floor(args):
                 for _ in range(args.warmup):
                     fn()
                 out[f"{name}_splits{sp}_us"] = round(_time_calls(torch, fn, args.steps, flush, stream) * 1e3, 2)
+        # the same flush and events around a one-element torch fill: the floor of any launch here
+        one = torch.empty(1, dtype=torch.int32, device=dev)
+        fill = lambda: one.fill_(1)
+        for _ in range(args.warmup):
+            fill()
+        out["trivial_kernel_us"] = round(_time_calls(torch, fill, args.steps, flush, stream) * 1e3, 2)
         out["full_gbs"] = round(out["bytes"] / (out[f"full_splits{heur}_us"] * 1e-6) / 1e9, 1)
         out["frac_hbm"] = round(out["full_gbs"] / peaks["hbm_gbs"], 4)
         print(json.dumps(out), flush=True)

@@ -153,3 +153,17 @@ def test_traced_call_records_an_ordered_timeline(attn):
         if c >= 2:  # a slot is refilled only after the chunk two back has left it
             assert cin >= tl[c - 2][2] - 1e-3, (c, tl[c], tl[c - 2])
     assert len(attn.attn_fwd_host_trace_read(capacity=3)) == 3
+
+
+def test_host_forward_with_the_pair_scheme(attn):
+    """The tile-scheme flag reaches the chunks' kernels: attn_fwd_host with
+    ATTN_FWD_CTA_PAIR gives the device call's result bit for bit."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N, d = 1, 8, 4, 900, 128
+    q, k, v = prefill_inputs(12, B, Hq, Hkv, N, d, dev)
+    o_dev, lse_dev = attn.forward(q, k, v, causal=True, tile_order=attn.FWD_CTA_PAIR)
+    hq, hk, hv = (_host(t, True) for t in (q, k, v))
+    o, lse = attn.forward_host(hq, hk, hv, causal=True, tile_order=attn.FWD_CTA_PAIR, kv_heads_per_chunk=1)
+    attn.check(attn.attn_device_status(), "device status")
+    assert torch.equal(o.view(torch.int16), o_dev.cpu().view(torch.int16))
+    assert torch.equal(lse, lse_dev.cpu())
