@@ -272,6 +272,11 @@ def run_gpu(args):
     dec_gbs = dec_bytes / dec_avg_s / 1e9
 
     fwd_bytes = fwd_traffic(B, H, N, d, causal, args.order)
+    long_step = fwd_avg_s * K >= 4.0  # the forward alone keeps the GPU busy for seconds
+    if long_step and peaks.get("bf16_tflops_sustained"):
+        peak_fwd, peak_kind = peaks["bf16_tflops_sustained"], "sustained (the forward runs back to back for seconds)"
+    else:
+        peak_fwd, peak_kind = peaks["bf16_tflops"], "burst"
     dec_traffic = decode_traffic(Bd, S, splits)
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
@@ -283,10 +288,15 @@ def run_gpu(args):
                    "tile_order": args.order, "decode_batch": Bd, "decode_kv_len": S,
                    "decode_splits": splits, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (no flush)"},
+        # The forward runs back to back for the whole timed region (about 0.8 s a
+        # launch at N = 131072, tens of seconds in all, under the power cap), so
+        # its denominator is the sustained bf16 figure; the burst fraction is
+        # reported beside it.
         "roofline": {"bound": "tensor", "achieved": round(per_gpu, 2),
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(per_gpu / peaks["bf16_tflops"], 4), "traffic": fwd_bytes,
-                     "peak_source": f"{peak_src} bf16 burst", "kernel": "fwd_kernel<128, false>",
+                     "peak": peak_fwd, "unit": "TFLOP/s",
+                     "frac": round(per_gpu / peak_fwd, 4), "traffic": fwd_bytes,
+                     "peak_source": f"{peak_src} bf16 {peak_kind}", "kernel": "fwd_kernel<128, false>",
+                     "frac_of_burst": round(per_gpu / peaks["bf16_tflops"], 4),
                      "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch "
                                         "with fewer heads at the same N, scaled by the head count"
                                         if fwd_bytes else None)},
