@@ -327,7 +327,11 @@ def run_gpu(args):
 
     # -- end to end through the C ABI with host buffers --
     if args.e2e and rank == 0:
-        hq_, hk_, hv_ = (t.cpu().pin_memory() for t in (q, k, v))
+        def pinned_copy(t):  # straight into page-locked memory (no pageable intermediate)
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            return h
+        hq_, hk_, hv_ = (pinned_copy(t) for t in (q, k, v))
         ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
         wbytes_h = attn.attn_fwd_host_workspace_bytes(B, H, H, N, d, 0)
