@@ -77,3 +77,21 @@ def test_reference_arm_is_silent_on_other_ranks():
                         "--steps", "1", "--ref-seconds", "0.2", "--n", "1024"],
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_timeline_summary_on_a_hand_made_timeline():
+    """Three chunks (copy-in done, kernel reached, kernel done, copy-out done,
+    ms from the call's start): kernels [1, 4], [3.5, 6] and [7, 9] -> busy
+    5 (the first two overlap) + 2 = 7 ms of a 10 ms call, one 1 ms gap,
+    chunk 2's copy-in ending 0.5 ms after chunk 1's kernel; with 4 ms of
+    copies alone, the call hid (7 + 4 - 10) / 4 of them."""
+    import bench
+    tl = [(1.0, 1.0, 4.0, 4.5), (2.0, 3.5, 6.0, 6.5), (6.5, 7.0, 9.0, 10.0)]
+    s = bench.timeline_summary(tl, 4.0)
+    assert s["chunks"] == 3 and s["wall_ms"] == 10.0
+    assert s["kernel_busy_ms"] == 7.0 and s["idle_ms"] == 3.0
+    assert s["kernel_ms_sum"] == 3.0 + 2.5 + 2.0
+    assert s["first_kernel_ms"] == 1.0 and s["after_last_kernel_ms"] == 1.0
+    assert s["max_gap_ms"] == 1.0
+    assert s["copy_in_late_ms"] == 0.5  # chunk 2 (6.5) after chunk 1's kernel (6.0); chunk 1 was early
+    assert s["overlap_frac"] == 0.25
