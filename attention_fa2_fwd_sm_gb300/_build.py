@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
 SOURCES = ["attn_api.cu", "fwd_sm103.cu", "fwd_pair_sm103.cu", "fwd_splitkv_sm103.cu", "fwd_host.cu", "decode_sm103.cu", "die_map.cu", "bwd_sm103.cu"]
-HEADERS = ["attn_internal.h", "sm103_ptx.cuh", "tile_order.cuh", "dkdv_order.cuh"]
+HEADERS = ["attn_internal.h", "fwd_kernel.cuh", "sm103_ptx.cuh", "tile_order.cuh", "dkdv_order.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I" + os.path.join(ROOT, "include")]
