@@ -250,6 +250,54 @@ __device__ __forceinline__ void tc_mma_ts_x4(uint32_t d, const uint32_t (&a)[4],
         : "memory");
 }
 
+// Warp-collective forms: all 32 lanes execute them together and the lane
+// that elect.sync picks (the lowest, the same one every time) issues the
+// instruction, so the issuing loop can run warp-uniform.
+__device__ __forceinline__ void tc_mma_ss_x4_elect(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4],
+                                                   uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %9, 0;\n\t"
+        "setp.eq.b32 p1, %9, %9;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %10, p0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %10, p1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %10, p1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %10, p1;\n\t}" ::"r"(d),
+        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0),
+        "r"(idesc)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_x4_elect(uint32_t d, const uint32_t (&a)[4], const uint64_t (&b)[4],
+                                                   uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %9, 0;\n\t"
+        "setp.eq.b32 p1, %9, %9;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %10, p0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %10, p1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %10, p1;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %10, p1;\n\t}" ::"r"(d),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0),
+        "r"(idesc)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
 // A K-major, B K-major (b_mn_major = 0) or MN-major (1), shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major) {
