@@ -76,7 +76,7 @@ constexpr int kTmemCols = 512;
 // (128 x 128 + 256 x 184 <= 384 x 168).  The host refuses a build whose
 // launch register count differs.
 constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 128;
+constexpr int kCtrlRegs = 136;
 constexpr int kEwRegs = 184;
 static_assert(128 * kCtrlRegs + 256 * kEwRegs <= kThreads * kLaunchRegs, "register split");
 
@@ -188,7 +188,8 @@ __device__ __forceinline__ void store_half_row(uint32_t t_row, int half, __nv_bf
 }
 
 // D (+)= A B^T over the head dimension (K-major A and B in 128-byte-swizzled
-// 64-column chunks), issued in groups of four MMAs from one asm block.
+// 64-column chunks), issued in groups of four MMAs from one asm block by
+// the warp's elected lane (the caller is the whole MMA warp).
 template <int D, int kChunkBytes>
 __device__ __forceinline__ void ss_product(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
 #pragma unroll
@@ -200,7 +201,7 @@ __device__ __forceinline__ void ss_product(uint32_t d_tmem, uint64_t a0, uint64_
             a[i] = a0 + off;
             b[i] = b0 + off;
         }
-        tc_mma_ss_x4(d_tmem, a, b, idesc, g > 0 ? 1u : 0u);
+        tc_mma_ss_x4_elect(d_tmem, a, b, idesc, g > 0 ? 1u : 0u);
     }
 }
 
@@ -218,7 +219,7 @@ __device__ __forceinline__ void ts_product(uint32_t d_tmem, uint32_t a_tmem, uin
             a[i] = a_tmem + kk * 8;
             b[i] = b0 + uint64_t((kk * 16 * 128) >> 4);
         }
-        tc_mma_ts_x4(d_tmem, a, b, idesc, (acc || g > 0) ? 1u : 0u);
+        tc_mma_ts_x4_elect(d_tmem, a, b, idesc, (acc || g > 0) ? 1u : 0u);
     }
 }
 
@@ -409,7 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         //   dVdK(0, t), S(0, t+1), dVdK(1, t), S(1, t+1)
         // so the tensor core works on one half while warpgroup h computes the
         // other, and the commit announcing S(h, t+1) also covers dVdK(h, t).
-        if (lane == 0) {
+        // The whole warp runs the issue loop (its state is warp-uniform); each
+        // MMA, commit and arrival goes out from one elected lane.
+        {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kRows, 64, 0);  // N = 64 query rows
             constexpr uint32_t kIdescAcc = idesc_bf16_f32(kRows, D, 1);  // B read MN-major
             const uint64_t dK0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int p_waits[2] = {0, 0};
             bool ok = true;
             auto wait_stage = [&](long long f) {
-                return mbar_wait_bounded(bar(C::kBarStFull + int(f % C::kStages)), uint32_t((f / C::kStages) & 1),
+                return mbar_wait_warp(bar(C::kBarStFull + int(f % C::kStages)), uint32_t((f / C::kStages) & 1),
                                          p.wait_ns, abort_flag, status);
             };
             // S^T_h and dP^T_h of the stage at ring position f.
@@ -431,19 +434,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tS = tmem_base + h * C::kColHalf;
                 ss_product<D, C::kChunkBytes>(tS, dK0, dQk, kIdescS);
                 ss_product<D, C::kChunkBytes>(tS + 64, dV0, dOk, kIdescS);
-                tc_commit(bar(C::kBarSFull + h));
+                tc_commit_elect(bar(C::kBarSFull + h));
             };
             for (long long qi = 0; ok; ++qi) {
                 const int qs = int(qi & 1);
-                ok = mbar_wait_bounded(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag,
+                ok = mbar_wait_warp(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag,
                                        status);
                 if (!ok) break;
-                const long long u = unit_q[qs];
-                mbar_arrive(bar(C::kBarUQEmpty + qs));
+                const long long u = __shfl_sync(0xffffffffu, int(unit_q[qs]), 0);
+                mbar_arrive_elect(bar(C::kBarUQEmpty + qs));
                 if (u < 0) break;
                 const KvUnit w = kv_unit(p, u);
                 const int iters = p.G * (p.nblk - kv_first_i(p, w.j));
-                ok = mbar_wait_bounded(bar(C::kBarKVFull), uint32_t(kv_used & 1), p.wait_ns, abort_flag, status);
+                ok = mbar_wait_warp(bar(C::kBarKVFull), uint32_t(kv_used & 1), p.wait_ns, abort_flag, status);
                 if (ok) ok = wait_stage(fills);
                 if (!ok) break;
                 ++kv_used;
@@ -454,12 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int slot = int(fills % C::kStages);
                     const bool has_next = t + 1 < iters;
                     for (int h = 0; h < 2; ++h) {
-                        ok = mbar_wait_bounded(bar(C::kBarPFull + h), uint32_t(p_waits[h] & 1), p.wait_ns,
+                        ok = mbar_wait_warp(bar(C::kBarPFull + h), uint32_t(p_waits[h] & 1), p.wait_ns,
                                                abort_flag, status);
                         if (!ok) break;
                         ++p_waits[h];
                         if (t == 0 && h == 0 && units_done > 0) {
-                            ok = mbar_wait_bounded(bar(C::kBarAccEmpty), uint32_t((units_done - 1) & 1), p.wait_ns,
+                            ok = mbar_wait_warp(bar(C::kBarAccEmpty), uint32_t((units_done - 1) & 1), p.wait_ns,
                                                    abort_flag, status);
                             if (!ok) break;
                         }
@@ -471,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const bool first = (t == 0 && h == 0);
                         ts_product<4>(tmem_base + C::kColDV, tH, dOmn, kIdescAcc, !first);  // K = 64 query rows
                         ts_product<4>(tmem_base + C::kColDK, tH + 64, dQmn, kIdescAcc, !first);
-                        if (h == 1) tc_commit(bar(C::kBarStEmpty + slot));
+                        if (h == 1) tc_commit_elect(bar(C::kBarStEmpty + slot));
                         if (has_next) {
                             if (h == 0) {
                                 ok = wait_stage(fills + 1);
@@ -484,15 +487,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     ++fills;
                     if (!has_next) {
-                        tc_commit(bar(C::kBarAccFull));
-                        tc_commit(bar(C::kBarKVEmpty));
+                        tc_commit_elect(bar(C::kBarAccFull));
+                        tc_commit_elect(bar(C::kBarKVEmpty));
                         ++units_done;
                     }
                 }
             }
-            tc_commit(bar(C::kBarDrain));
+            tc_commit_elect(bar(C::kBarDrain));
             volatile int no_abort = 0;
-            if (!mbar_wait_bounded(bar(C::kBarDrain), 0, 1000000000ull, &no_abort, status))
+            if (!mbar_wait_warp(bar(C::kBarDrain), 0, 1000000000ull, &no_abort, status) && lane == 0)
                 atomicOr(status, kStatusDrainTimeout);
         }
         __syncwarp();
@@ -852,7 +855,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the issue loop (its state is warp-uniform); each
+        // MMA, commit and arrival goes out from one elected lane.
+        {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kRows, kRows, 0);
             constexpr uint32_t kIdescAcc = idesc_bf16_f32(kRows, D, 1);
             long long fills = 0;
@@ -860,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             auto slot_of = [&](long long f) { return dq_slot<D>(f); };
             auto wait_fill = [&](long long f) {
-                return mbar_wait_bounded(bar(C::kBarKVFull + slot_of(f)), uint32_t(dq_use<D>(f) & 1), p.wait_ns,
+                return mbar_wait_warp(bar(C::kBarKVFull + slot_of(f)), uint32_t(dq_use<D>(f) & 1), p.wait_ns,
                                          abort_flag, status);
             };
             auto kmaj = [&](long long f) { return smem_desc_sw128(smem_u32(sKV + slot_of(f) * C::kTileBytes), 16, 1024); };
@@ -868,22 +873,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ss_product<D, C::kChunkBytes>(tmem_base + kRows * t,
                                               smem_desc_sw128(smem_u32(sQ + t * C::kTileBytes), 16, 1024), kmaj(fK),
                                               kIdescS);
-                tc_commit(bar(C::kBarSFull + t));
+                tc_commit_elect(bar(C::kBarSFull + t));
             };
             for (long long qi = 0; ok; ++qi) {
                 const int qs = int(qi & 1);
-                ok = mbar_wait_bounded(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag,
+                ok = mbar_wait_warp(bar(C::kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, abort_flag,
                                        status);
                 if (!ok) break;
-                const long long u = unit_q[qs];
-                mbar_arrive(bar(C::kBarUQEmpty + qs));
+                const long long u = __shfl_sync(0xffffffffu, int(unit_q[qs]), 0);
+                mbar_arrive_elect(bar(C::kBarUQEmpty + qs));
                 if (u < 0) break;
                 const QUnit2 w = q_unit2(p, u);
                 const long long f0 = fills;  // K_j at f0 + 2 j, V_j at f0 + 2 j + 1
                 ok = wait_fill(f0);
                 for (int t = 0; ok && t < 2; ++t) {
                     if (w.nkv[t] == 0) continue;
-                    ok = mbar_wait_bounded(bar(C::kBarQFull + t), uint32_t(q_used[t] & 1), p.wait_ns, abort_flag,
+                    ok = mbar_wait_warp(bar(C::kBarQFull + t), uint32_t(q_used[t] & 1), p.wait_ns, abort_flag,
                                            status);
                     if (!ok) break;
                     ++q_used[t];
@@ -896,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = wait_fill(fV);
                     for (int t = 0; ok && t < 2; ++t) {
                         if (j >= w.nkv[t]) continue;
-                        ok = mbar_wait_bounded(bar(C::kBarPFull + t), uint32_t(p_waits[t] & 1), p.wait_ns, abort_flag,
+                        ok = mbar_wait_warp(bar(C::kBarPFull + t), uint32_t(p_waits[t] & 1), p.wait_ns, abort_flag,
                                                status);
                         if (!ok) break;
                         ++p_waits[t];
@@ -904,20 +909,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ss_product<D, C::kChunkBytes>(tmem_base + kRows * t,
                                                       smem_desc_sw128(smem_u32(sDO + t * C::kTileBytes), 16, 1024),
                                                       kmaj(fV), kIdescS);
-                        tc_commit(bar(C::kBarDPFull + t));
+                        tc_commit_elect(bar(C::kBarDPFull + t));
                     }
                     if (!ok) break;
-                    tc_commit(bar(C::kBarKVEmpty + slot_of(fV)));  // V_j consumed
+                    tc_commit_elect(bar(C::kBarKVEmpty + slot_of(fV)));  // V_j consumed
                     // dQ(t, j) once warpgroup t wrote dS, then S(t, j + 1)
                     bool k_next = false;
                     for (int t = 0; ok && t < 2; ++t) {
                         if (j >= w.nkv[t]) continue;
-                        ok = mbar_wait_bounded(bar(C::kBarDSFull + t), uint32_t(ds_waits[t] & 1), p.wait_ns,
+                        ok = mbar_wait_warp(bar(C::kBarDSFull + t), uint32_t(ds_waits[t] & 1), p.wait_ns,
                                                abort_flag, status);
                         if (!ok) break;
                         ++ds_waits[t];
                         if (j == 0 && units_done[t] > 0) {
-                            ok = mbar_wait_bounded(bar(C::kBarAccEmpty + t), uint32_t((units_done[t] - 1) & 1),
+                            ok = mbar_wait_warp(bar(C::kBarAccEmpty + t), uint32_t((units_done[t] - 1) & 1),
                                                    p.wait_ns, abort_flag, status);
                             if (!ok) break;
                         }
@@ -934,19 +939,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             issue_s(t, fK + 2);
                         } else {
-                            tc_commit(bar(C::kBarAccFull + t));  // dQ(t) final for this unit
-                            tc_commit(bar(C::kBarQEmpty + t));   // Q_t, dO_t reusable
+                            tc_commit_elect(bar(C::kBarAccFull + t));  // dQ(t) final for this unit
+                            tc_commit_elect(bar(C::kBarQEmpty + t));   // Q_t, dO_t reusable
                             ++units_done[t];
                         }
                     }
                     if (!ok) break;
-                    tc_commit(bar(C::kBarKVEmpty + slot_of(fK)));  // K_j consumed
+                    tc_commit_elect(bar(C::kBarKVEmpty + slot_of(fK)));  // K_j consumed
                 }
                 fills = f0 + 2 * (long long)w.nmax;
             }
-            tc_commit(bar(C::kBarDrain));
+            tc_commit_elect(bar(C::kBarDrain));
             volatile int no_abort = 0;
-            if (!mbar_wait_bounded(bar(C::kBarDrain), 0, 1000000000ull, &no_abort, status))
+            if (!mbar_wait_warp(bar(C::kBarDrain), 0, 1000000000ull, &no_abort, status) && lane == 0)
                 atomicOr(status, kStatusDrainTimeout);
         }
         __syncwarp();

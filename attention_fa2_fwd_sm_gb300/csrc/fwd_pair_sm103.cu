@@ -68,7 +68,7 @@ constexpr int kBlockN = 128;          // keys per K/V block
 constexpr int kNT = 2;                // pair tiles per unit
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 104;
+constexpr int kCtrlRegs = 120;  // the warp-wide MMA issue loop spills at 104
 constexpr int kSoftmaxRegs = 192;
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kTmemCols = 512;
@@ -265,6 +265,54 @@ __device__ __forceinline__ void mma_ts_x4_pair(uint32_t d, const uint32_t (&a)[4
         "tcgen05.mma.cta_group::2.kind::f16 [%0], [%2], %6, %10, p1;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], [%3], %7, %10, p1;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], [%4], %8, %10, p1;\n\t}" ::"r"(d),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0),
+        "r"(idesc)
+        : "memory");
+}
+
+// Warp-collective forms of the above: all 32 lanes execute them and the lane
+// that elect.sync picks (the lowest, the same one every time) issues.
+__device__ __forceinline__ void commit_both_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
+        ::"r"(bar), "h"(kBothCtas)
+        : "memory");
+}
+__device__ __forceinline__ void commit_local_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ss_x4_pair_elect(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4],
+                                                     uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %9, 0;\n\t"
+        "setp.eq.b32 p1, %9, %9;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %5, %10, p0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %2, %6, %10, p1;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %3, %7, %10, p1;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %4, %8, %10, p1;\n\t}" ::"r"(d),
+        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0),
+        "r"(idesc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_x4_pair_elect(uint32_t d, const uint32_t (&a)[4], const uint64_t (&b)[4],
+                                                     uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %9, 0;\n\t"
+        "setp.eq.b32 p1, %9, %9;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %5, %10, p0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%2], %6, %10, p1;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%3], %7, %10, p1;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%4], %8, %10, p1;\n\t}" ::"r"(d),
         "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0),
         "r"(idesc)
         : "memory");
@@ -505,7 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issuer
-        if (lane == 0 && rank == 0) {
+        // Rank 0's whole warp runs the issue loop (its state is warp-uniform);
+        // each MMA, commit and arrival goes out from one elected lane.
+        if (rank == 0) {
             constexpr uint32_t kIdescQK = idesc_bf16_f32(2 * kTileM, kBlockN, 0);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(2 * kTileM, D, 1);
             long long fills = 0;
@@ -515,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
 
             auto wait_slot = [&](long long f) {
-                return wait_pair(bar(kBarKVFull + int(f % kStages)), uint32_t((f / kStages) & 1), p.wait_ns, ab);
+                return wait_pair_warp(bar(kBarKVFull + int(f % kStages)), uint32_t((f / kStages) & 1), p.wait_ns, ab);
             };
             const uint64_t dQ = smem_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dK = smem_desc_sw128(smem_u32(sKV), 16, 1024);
@@ -533,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         a[i] = a0 + uint64_t((g * kQChunkBytes + i * 32) >> 4);
                         b[i] = b0 + uint64_t((g * kKChunkBytes + i * 32) >> 4);
                     }
-                    mma_ss_x4_pair(d_tmem, a, b, kIdescQK, g > 0 ? 1u : 0u);
+                    mma_ss_x4_pair_elect(d_tmem, a, b, kIdescQK, g > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, long long fV, bool acc) {
@@ -550,39 +600,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                         a[i] = a_tmem + kk * 8;
                         b[i] = b0 + uint64_t((kk * 16 * 128) >> 4);
                     }
-                    mma_ts_x4_pair(d_tmem, a, b, kIdescPV, (acc || g > 0) ? 1u : 0u);
+                    mma_ts_x4_pair_elect(d_tmem, a, b, kIdescPV, (acc || g > 0) ? 1u : 0u);
                 }
             };
 
             for (long long qi = 0; ok; ++qi) {
                 const int qs = int(qi & 1);
-                ok = wait_pair(bar(kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, ab);
+                ok = wait_pair_warp(bar(kBarUQFull + qs), uint32_t((qi >> 1) & 1), p.wait_ns, ab);
                 if (!ok) break;
-                const long long u = unit_q[qs];
-                mbar_arrive(bar(kBarUQEmpty + qs));
+                const long long u = __shfl_sync(0xffffffffu, int(unit_q[qs]), 0);
+                mbar_arrive_elect(bar(kBarUQEmpty + qs));
                 if (u < 0) break;
                 const UnitWork w = unit_work<kGrouped>(p, u);
                 const long long f0 = fills;
                 ok = wait_slot(f0);
                 for (int t = 0; ok && t < kNT; ++t) {
                     if (w.nkv[t] == 0) continue;
-                    ok = wait_pair(bar(kBarQFull + t), q_used[t] & 1, p.wait_ns, ab);
+                    ok = wait_pair_warp(bar(kBarQFull + t), q_used[t] & 1, p.wait_ns, ab);
                     if (!ok) break;
                     ++q_used[t];
                     tc_fence_after();
                     issue_qk(t, f0);
-                    commit_both(bar(kBarSFull + t));
+                    commit_both_elect(bar(kBarSFull + t));
                 }
                 for (int j = 0; ok && j < w.nmax; ++j) {
                     const long long fV = f0 + 2 * j + 1, fK = f0 + 2 * j + 2;
                     bool v_ready = false, k_ready = false;
                     for (int t = 0; ok && t < kNT; ++t) {
                         if (j >= w.nkv[t]) continue;
-                        ok = wait_pair(bar(kBarPFull + t), p_waits[t] & 1, p.wait_ns, ab);
+                        ok = wait_pair_warp(bar(kBarPFull + t), p_waits[t] & 1, p.wait_ns, ab);
                         if (!ok) break;
                         ++p_waits[t];
                         if (j == 0 && units_done[t] > 0) {
-                            ok = wait_pair(bar(kBarOEmpty + t), (units_done[t] - 1) & 1, p.wait_ns, ab);
+                            ok = wait_pair_warp(bar(kBarOEmpty + t), (units_done[t] - 1) & 1, p.wait_ns, ab);
                             if (!ok) break;
                         }
                         if (!v_ready) {
@@ -592,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_fence_after();
                         issue_pv(t, fV, j > 0);
-                        if (t == last_user(w, j)) commit_both(bar(kBarKVEmpty + int(fV % kStages)));
+                        if (t == last_user(w, j)) commit_both_elect(bar(kBarKVEmpty + int(fV % kStages)));
                         if (j + 1 < w.nkv[t]) {
                             if (!k_ready) {
                                 ok = wait_slot(fK);
@@ -600,19 +650,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 k_ready = true;
                             }
                             issue_qk(t, fK);
-                            commit_both(bar(kBarSFull + t));
+                            commit_both_elect(bar(kBarSFull + t));
                         } else {
-                            commit_both(bar(kBarOFull + t));
-                            commit_both(bar(kBarQEmpty + t));
+                            commit_both_elect(bar(kBarOFull + t));
+                            commit_both_elect(bar(kBarQEmpty + t));
                             ++units_done[t];
                         }
                     }
                 }
                 fills = f0 + 2 * (long long)w.nmax;
             }
-            commit_local(bar(kBarDrain));
+            commit_local_elect(bar(kBarDrain));
             volatile int no_abort = 0;
-            if (!mbar_wait_bounded(bar(kBarDrain), 0, 1000000000ull, &no_abort, status))
+            if (!mbar_wait_warp(bar(kBarDrain), 0, 1000000000ull, &no_abort, status) && lane == 0)
                 atomicOr(status, kStatusDrainTimeout);
         }
         __syncwarp();
