@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (V slots keep their commit right after the last PV that reads them:
         // waiting for the next S would free them about eight MMAs later, which
         // measured slower.)
-        const bool frees_slots = (quarter == 0 && lane == 0);
+        const bool frees_slots = (quarter == 0);  // warp-uniform; the elected lane arrives
         bool ok = true;
 
         for (long long qi = 0; ok; ++qi) {
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             const long long u = unit_q[qs];
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarUQEmpty + qs));
+            mbar_arrive_elect(bar(C::kBarUQEmpty + qs));
             if (u < 0) break;
             const auto w = unit_work<kMap>(p, u);
             const long long f0 = kv_base;  // K_j at ring position f0 + 2j
@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 ++s_waits;
                 if (frees_slots && t == last_user(w, j))
-                    mbar_arrive(bar(C::kBarKVEmpty + int((f0 + 2 * j) % C::kStages)));
+                    mbar_arrive_elect(bar(C::kBarKVEmpty + int((f0 + 2 * j) % C::kStages)));
                 tc_fence_after();
                 uint32_t sr[4][32];
 #pragma unroll
@@ -670,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::kBarPFull + t));
+                mbar_arrive_elect(bar(C::kBarPFull + t));
             }
             if (!ok) break;
 
@@ -734,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarOEmpty + t));
+            mbar_arrive_elect(bar(C::kBarOEmpty + t));
         }
     }
 
