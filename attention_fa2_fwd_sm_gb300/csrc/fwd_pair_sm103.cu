@@ -774,19 +774,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                     l_blk = exp_block(m_run == -INFINITY ? 0.f : -m_run);
-                }
-                l_run = l_run * corr + l_blk;
-                if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+                    // O moves only when the maximum does, so its rescale is checked
+                    // here, off the common path.
+                    if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(tO + c * 32, ov);
-                        tmem_wait_ld();
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t ov[32];
+                            tmem_ld32(tO + c * 32, ov);
+                            tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
-                        tmem_st32(tO + c * 32, ov);
+                            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
+                            tmem_st32(tO + c * 32, ov);
+                        }
                     }
                 }
+                l_run = l_run * corr + l_blk;
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
