@@ -43,6 +43,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -66,6 +68,26 @@ static std::atomic<unsigned int> g_bwd_launch_seq{0};
 
 namespace bwd {
 
+// (d0, d1) = (a0 - b0, a1 - b1) and (a0 * b0, a1 * b1) as paired fp32 operations.
+__device__ __forceinline__ void fsub2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fmul2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 constexpr int kRows = 128;     // rows per tile (keys in dkdv, queries in dq)
 constexpr int kThreads = 384;  // 12 warps: 4 control, 8 elementwise
 constexpr int kEwWarps = 8;    // two per TMEM lane quarter, each on half of the columns
@@ -82,7 +104,7 @@ static_assert(128 * kCtrlRegs + 256 * kEwRegs <= kThreads * kLaunchRegs, "regist
 
 struct Params {
     __nv_bfloat16 *out0, *out1;  // dkdv: dK, dV; dq: dQ (out1 unused)
-    const float *lse2;           // [B*Hq, npad]  lse * log2(e), +inf past N
+    const float *nlse2;          // [B*Hq, npad]  -lse * log2(e), -inf past N
     const float *delta;          // [B*Hq, npad]  rowsum(dO * O), 0 past N
     int B, N, npad, Hq, Hkv, G, d_store, causal, order, nblk;
     int kv_window;  // dkdv head-first: (batch, KV head) pairs interleaved per window
@@ -95,10 +117,11 @@ struct Params {
 // ------------------------------------------------------------------ pre-pass
 
 // One warp per padded query row: Delta = sum_c dO[c] * O[c] (fp32) and
-// lse * log2(e); rows at or past N get +inf and 0.
+// -lse * log2(e) (negated, so the exponent argument is one FMA); rows at or
+// past N get -inf and 0.
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ dout,
-                                                      const float *__restrict__ lse, float *lse2,
+                                                      const float *__restrict__ lse, float *nlse2,
                                                       float *delta, int N, int npad, int d,
                                                       long long rows) {
     const int lane = threadIdx.x & 31;
@@ -109,7 +132,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
         const int n = int(r % npad);
         if (n >= N) {
             if (lane == 0) {
-                lse2[r] = INFINITY;
+                nlse2[r] = -INFINITY;
                 delta[r] = 0.f;
             }
             continue;
@@ -126,7 +149,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) {
-            lse2[r] = lse[(size_t)bh * N + n] * 1.4426950408889634f;
+            nlse2[r] = -(lse[(size_t)bh * N + n] * 1.4426950408889634f);
             delta[r] = acc;
         }
     }
@@ -241,7 +264,7 @@ struct KvCfg {
     static constexpr int kChunkBytes = kRows * 128;    // one chunk of 128 rows
     static constexpr int kTileBytes = kRows * D * 2;   // one 128 x D bf16 tile
     static constexpr int kStages = (D == 128) ? 2 : 3; // Q/dO ring
-    static constexpr int kStageBytes = 2 * kTileBytes + 1024;  // Q, dO, lse2, Delta
+    static constexpr int kStageBytes = 2 * kTileBytes + 1024;  // Q, dO, -lse2, Delta
     // barriers: kv_full kv_empty st_full[S] st_empty[S] s_full[2] p_full[2]
     //           acc_full acc_empty uq_full[2] uq_empty[2] drain
     static constexpr int kBarKVFull = 0, kBarKVEmpty = 1, kBarStFull = 2, kBarStEmpty = 2 + kStages,
@@ -378,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     i * kRows, bh);
                     }
                     const size_t row0 = (size_t)bh * p.npad + (size_t)i * kRows;
-                    bulk_load(smem_u32(stage_l(slot)), p.lse2 + row0, kRows * 4, fb);
+                    bulk_load(smem_u32(stage_l(slot)), p.nlse2 + row0, kRows * 4, fb);
                     bulk_load(smem_u32(stage_l(slot) + kRows), p.delta + row0, kRows * 4, fb);
                     ++fills;
                 }
@@ -549,39 +572,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float4 *d4 = reinterpret_cast<const float4 *>(stage_l(slot) + kRows) + half * 16;
                 const bool diag = p.causal && i == w.j;  // query rows before this key are masked
                 tmem_wait_ld();
+                // P^T = 2^(S^T * scale * log2 e - lse2) and dS^T = P^T (dP^T - Delta),
+                // written as bf16 over the half's columns.  The causal mask
+                // (query rows before this key) applies only on the diagonal
+                // block, so that block has its own copy of the loop.
+                auto elementwise = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int q0 = half * 64 + c * 32;  // first query row of the chunk
-                    uint32_t pk[16], dk[16];
+                    for (int c = 0; c < 2; ++c) {
+                        const int q0 = half * 64 + c * 32;  // first query row of the chunk
+                        uint32_t pk[16], dk[16];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 L = l4[c * 8 + e];
-                        const float4 Dl = d4[c * 8 + e];
-                        const float lv[4] = {L.x, L.y, L.z, L.w};
-                        const float dl[4] = {Dl.x, Dl.y, Dl.z, Dl.w};
-                        float pr[4], ds[4];
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 L = l4[c * 8 + e];   // -lse2
+                            const float4 Dl = d4[c * 8 + e];  // Delta
+                            const float nl[4] = {L.x, L.y, L.z, L.w};
+                            const float dl[4] = {Dl.x, Dl.y, Dl.z, Dl.w};
+                            float pr[4], ds[4];
 #pragma unroll
-                        for (int k = 0; k < 4; k += 2) {
-                            float x0, x1;
-                            ffma2(x0, x1, __uint_as_float(sv[c][4 * e + k]), __uint_as_float(sv[c][4 * e + k + 1]),
-                                  sl2, sl2, -lv[k], -lv[k + 1]);
-                            pr[k] = fast_exp2(x0);
-                            pr[k + 1] = fast_exp2(x1);
+                            for (int k = 0; k < 4; k += 2) {
+                                float x0, x1;
+                                ffma2(x0, x1, __uint_as_float(sv[c][4 * e + k]), __uint_as_float(sv[c][4 * e + k + 1]),
+                                      sl2, sl2, nl[k], nl[k + 1]);
+                                pr[k] = fast_exp2(x0);
+                                pr[k + 1] = fast_exp2(x1);
+                            }
+                            if constexpr (decltype(masked)::value) {
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    if (q0 + 4 * e + k < r) pr[k] = 0.f;
+                            }
+#pragma unroll
+                            for (int k = 0; k < 4; k += 2) {
+                                float t0, t1;
+                                fsub2(t0, t1, __uint_as_float(dv[c][4 * e + k]), __uint_as_float(dv[c][4 * e + k + 1]),
+                                      dl[k], dl[k + 1]);
+                                fmul2(ds[k], ds[k + 1], pr[k], pr[k + 1], t0, t1);
+                            }
+                            pk[2 * e] = pack_bf16x2(pr[0], pr[1]);
+                            pk[2 * e + 1] = pack_bf16x2(pr[2], pr[3]);
+                            dk[2 * e] = pack_bf16x2(ds[0], ds[1]);
+                            dk[2 * e + 1] = pack_bf16x2(ds[2], ds[3]);
                         }
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            if (diag && q0 + 4 * e + k < r) pr[k] = 0.f;
-                            ds[k] = pr[k] * (__uint_as_float(dv[c][4 * e + k]) - dl[k]);
-                        }
-                        pk[2 * e] = pack_bf16x2(pr[0], pr[1]);
-                        pk[2 * e + 1] = pack_bf16x2(pr[2], pr[3]);
-                        dk[2 * e] = pack_bf16x2(ds[0], ds[1]);
-                        dk[2 * e + 1] = pack_bf16x2(ds[2], ds[3]);
+                        // bf16 pairs over the half's own fp32 columns, all read above
+                        tmem_st16(tH + c * 16, pk);
+                        tmem_st16(tH + 64 + c * 16, dk);
                     }
-                    // bf16 pairs over the half's own fp32 columns, all read above
-                    tmem_st16(tH + c * 16, pk);
-                    tmem_st16(tH + 64 + c * 16, dk);
-                }
+                };
+                if (diag)
+                    elementwise(std::true_type{});
+                else
+                    elementwise(std::false_type{});
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -982,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nkv == 0) continue;
             const int row = w.row0[t] + r;
             const size_t prow = (size_t)(w.b * p.Hq + w.h) * p.npad + row;  // row < npad always
-            const float neg_l = -p.lse2[prow];                               // -inf past N
+            const float neg_l = p.nlse2[prow];                               // -inf past N
             const float del = p.delta[prow];
             for (int j = 0; j < nkv; ++j) {
                 // P = exp(S - lse), kept in registers
@@ -1000,17 +1040,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int lim = kRows;  // block columns c >= lim are masked (past N or after the row)
                     if (kv0 + kRows > p.N) lim = p.N - kv0;
                     if (p.causal && j == w.row0[t] / kRows) lim = min(lim, r + 1);
+                    // Only the last block and the diagonal one mask columns; the
+                    // others take the loop without the per-column selects.
+                    auto exps = [&](auto masked) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                        for (int c = 0; c < 4; ++c)
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            float x0, x1;
-                            ffma2(x0, x1, __uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1]), sl2, sl2,
-                                  neg_l, neg_l);
-                            const int k = c * 32 + 2 * e;
-                            pr[k] = k < lim ? fast_exp2(x0) : 0.f;
-                            pr[k + 1] = k + 1 < lim ? fast_exp2(x1) : 0.f;
-                        }
+                            for (int e = 0; e < 16; ++e) {
+                                float x0, x1;
+                                ffma2(x0, x1, __uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1]), sl2,
+                                      sl2, neg_l, neg_l);
+                                const int k = c * 32 + 2 * e;
+                                if constexpr (decltype(masked)::value) {
+                                    pr[k] = k < lim ? fast_exp2(x0) : 0.f;
+                                    pr[k + 1] = k + 1 < lim ? fast_exp2(x1) : 0.f;
+                                } else {
+                                    pr[k] = fast_exp2(x0);
+                                    pr[k + 1] = fast_exp2(x1);
+                                }
+                            }
+                    };
+                    if (__any_sync(0xffffffffu, lim < kRows))
+                        exps(std::true_type{});
+                    else
+                        exps(std::false_type{});
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -1027,9 +1080,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16x2(pr[c * 32 + 2 * e] * (__uint_as_float(dv[2 * e]) - del),
-                                            pr[c * 32 + 2 * e + 1] * (__uint_as_float(dv[2 * e + 1]) - del));
+                    for (int e = 0; e < 16; ++e) {
+                        float t0, t1, d0, d1;
+                        fsub2(t0, t1, __uint_as_float(dv[2 * e]), __uint_as_float(dv[2 * e + 1]), del, del);
+                        fmul2(d0, d1, pr[c * 32 + 2 * e], pr[c * 32 + 2 * e + 1], t0, t1);
+                        pk[e] = pack_bf16x2(d0, d1);
+                    }
                     tmem_st16(tX + c * 16, pk);  // over columns already read
                 }
                 tmem_wait_st();
@@ -1068,7 +1124,7 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
     const int nblk = (a.N + kRows - 1) / kRows;
     const int npad = nblk * kRows;
     const long long rows = (long long)a.B * a.Hq * npad;
-    float *lse2 = a.workspace;
+    float *nlse2 = a.workspace;
     float *delta = a.workspace + rows;
 
     // Pre-pass: Delta and lse * log2(e).
@@ -1078,7 +1134,7 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
         if (blocks > cap) blocks = cap;
         bwd_pre_kernel<<<unsigned(blocks), 256, 0, stream>>>(
             reinterpret_cast<const __nv_bfloat16 *>(a.o), reinterpret_cast<const __nv_bfloat16 *>(a.dout), a.lse,
-            lse2, delta, a.N, npad, a.d, rows);
+            nlse2, delta, a.N, npad, a.d, rows);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return note_cuda_error(e, "bwd_pre_kernel launch");
     }
@@ -1111,7 +1167,7 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
         if (dev >= 0) attr_set[dev] = true;
     }
     Params p;
-    p.lse2 = lse2;
+    p.nlse2 = nlse2;
     p.delta = delta;
     p.B = a.B;
     p.N = a.N;

@@ -245,7 +245,7 @@ long long attn_fwd_host_trace_read(float *ms, long long capacity);
  *   d in {56, 64, 128} as in attn_fwd; tile_order HEAD_FIRST, BLOCK_FIRST or
  *   NAIVE_HEAD_FIRST (the die-split order is forward-only).
  *   workspace: device memory of at least attn_bwd_workspace_bytes(B, Hq, N)
- *   bytes, 16-byte aligned; it receives lse * log2(e) and Delta per query row.
+ *   bytes, 16-byte aligned; it receives -lse * log2(e) and Delta per query row.
  * Three kernels run on `stream`: the Delta pre-pass, the dK/dV pass (units of
  * 128 keys of one KV head) and the dQ pass (units of 256 query rows of one
  * query head); the two main passes are persistent grids that take units in
