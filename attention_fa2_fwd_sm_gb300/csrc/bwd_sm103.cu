@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(C::kBarAccEmpty), kEwWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(C::kBarUQFull + i), 1);
-            mbar_init(bar(C::kBarUQEmpty + i), 1 + kEwWarps);  // MMA thread + elementwise warps
+            mbar_init(bar(C::kBarUQEmpty + i), 1 + kEwWarps);  // MMA warp + elementwise warps
         }
         mbar_init(bar(C::kBarDrain), 1);
         *abort_flag = 0;
@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = int(fills % C::kStages);
                 ok = mbar_wait_warp(bar(C::kBarSFull + half), uint32_t(s_waits & 1), p.wait_ns, abort_flag, status);
                 // The stage's lse / Delta rows: wait on the stage's own fill barrier
-                // (already complete, since the MMA thread waited on it first).
+                // (already complete, since the MMA warp waited on it first).
                 if (ok)
                     ok = mbar_wait_warp(bar(C::kBarStFull + slot), uint32_t((fills / C::kStages) & 1), p.wait_ns,
                                         abort_flag, status);
@@ -679,7 +679,7 @@ struct QCfg {
     // K/V ring of single tiles.  K tiles and V tiles have rings of their own:
     // V_j is free once both dP products of block j are done, early in the
     // block, while K_j is read by the block's last dQ product; sharing one
-    // round-robin ring put V_j+1 into K_j's slot and the MMA thread waited for
+    // round-robin ring put V_j+1 into K_j's slot and the MMA warp waited for
     // it at the start of every block.
     static constexpr int kKSlots = (D == 128) ? 2 : 4;
     static constexpr int kVSlots = (D == 128) ? 1 : 2;

@@ -1,5 +1,5 @@
 // fwd_pair_sm103.cu -- the forward (prefill) kernel on CTA pairs: tcgen05
-// MMAs of the cta_group::2 kind, M = 256, issued by one thread for two SMs.
+// MMAs of the cta_group::2 kind, M = 256, issued by one warp for two SMs.
 //
 // Same computation as fwd_sm103.cu -- O = softmax(scale * Q K^T) V and lse
 // per query row ("Optimizing Attention on GPUs by Exploiting GPU
@@ -22,17 +22,18 @@
 //                        each CTA supplies d/2 of V's columns (B); each CTA's
 //                        TMEM receives its rows' O for all d columns.
 // So each SM loads half of every K/V block (16 KiB of K, 16 KiB of V at
-// d = 128) and the pair's MMA thread issues one instruction per 256 rows.
+// d = 128) and the pair's MMA warp issues one instruction per 256 rows.
 //
 // Roles (384 threads per CTA, as in the one-CTA kernel):
 //   warp 0      TMA producer of this CTA's halves (both CTAs).  Copies complete
 //               on the rank-0 CTA's barriers (the .cta_group::2 form of the
 //               tensor copy), which count both halves' bytes.
-//   warp 1      rank 0: the MMA thread of the pair; rank 1: TMEM only.
+//   warp 1      rank 0: the MMA warp of the pair (the whole warp runs the loop,
+//               an elected lane issues); rank 1: TMEM only.
 //   warps 4-11  softmax / epilogue of this CTA's rows of pair tiles 0 and 1.
 // Rank 0 fetches the units and hands them to rank 1 through its shared
-// memory.  The MMA thread's commits arrive on both CTAs' barriers
-// (multicast); the softmax warps of both CTAs hand P to the MMA thread on
+// memory.  The MMA warp's commits arrive on both CTAs' barriers
+// (multicast); the softmax warps of both CTAs hand P to the MMA warp on
 // rank 0's barriers.  Every wait is bounded in time; a wait that gives up
 // sets both CTAs' abort flags.
 #include <cuda_bf16.h>
@@ -92,7 +93,7 @@ constexpr int kBarQFull = 0,          // [2] r0: both CTAs' Q halves landed
     kBarUQFull = 13 + 2 * kStages,    // [2] both: unit queue entry written
     kBarUQEmpty = 15 + 2 * kStages,   // [2] r0: entry read by every role of the pair
     kNumBars = 17 + 2 * kStages;
-constexpr int kUQConsumers = 2 * (1 + 8);  // per CTA: producer or MMA thread, and 8 softmax warps
+constexpr int kUQConsumers = 2 * (1 + 8);  // per CTA: producer or MMA warp, and 8 softmax warps
 constexpr int kDataBytes = kNT * kQBytes + kStages * kHalfBytes;
 constexpr int kSmemBytes = kDataBytes + kNumBars * 8 + 32 + 1024;
 constexpr uint16_t kBothCtas = 0x3;

@@ -96,7 +96,7 @@ enum attn_tile_order {
  *    MMA tiles sharing every K/V block it loads).
  *  ATTN_FWD_CTA_PAIR: pairs of SMs (a cluster of two CTAs) run units of 512
  *    query rows with tcgen05 MMAs of the cta_group::2 kind (M = 256): each SM
- *    loads half of every K/V block and one thread issues the MMAs of both.
+ *    loads half of every K/V block and one warp issues the MMAs of both.
  *    The pages keep the workgroups that share one head's K/V on one chiplet
  *    (detail page, section 2 Q1-Q2); a pair shares each block through the
  *    MMA itself.  d = 128 only (ATTN_ERR_UNSUPPORTED otherwise).  The units
