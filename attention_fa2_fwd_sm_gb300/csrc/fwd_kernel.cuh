@@ -1,4 +1,4 @@
-// fwd_kernel.cuh -- FlashAttention-2 style forward (prefill) kernel body for sm_103a.
+// fwd_kernel.cuh -- FlashAttention-2 style forward (prefill) kernel for sm_103a.
 //
 // Computes O = softmax(scale * Q K^T) V and lse per query row ("Optimizing
 // Attention on GPUs by Exploiting GPU Architectural NUMA Effects", detail

@@ -29,8 +29,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-__device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
-
 // --------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -185,74 +183,15 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Make all prior tcgen05 async operations of this thread arrive on `bar` once complete.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T  (kind::f16, one CTA)
-__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]  (kind::f16, one CTA, A read from tensor memory)
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Groups of MMAs issued from one asm block: the issuing thread then spends no
-// instructions between consecutive tcgen05.mma, which matters when other
-// warps of its SM sub-partition keep the issue slots busy.  `acc0` enables
-// accumulation for the first MMA; the later ones always accumulate.
-// SS: a[i], b[i] are the shared-memory descriptors of MMA i.
-__device__ __forceinline__ void tc_mma_ss_x4(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4],
-                                             uint32_t idesc, uint32_t acc0) {
-    asm volatile(
-        "{\n\t.reg .pred p0, p1;\n\t"
-        "setp.ne.b32 p0, %9, 0;\n\t"
-        "setp.eq.b32 p1, %9, %9;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %10, p0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %10, p1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %10, p1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %10, p1;\n\t}" ::"r"(d),
-        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0),
-        "r"(idesc)
-        : "memory");
-}
-
-// TS: a[i] are the TMEM addresses of A, b[i] the shared-memory descriptors of B.
-__device__ __forceinline__ void tc_mma_ts_x4(uint32_t d, const uint32_t (&a)[4], const uint64_t (&b)[4],
-                                             uint32_t idesc, uint32_t acc0) {
-    asm volatile(
-        "{\n\t.reg .pred p0, p1;\n\t"
-        "setp.ne.b32 p0, %9, 0;\n\t"
-        "setp.eq.b32 p1, %9, %9;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %10, p0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %10, p1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %10, p1;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %10, p1;\n\t}" ::"r"(d),
-        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc0),
-        "r"(idesc)
-        : "memory");
-}
-
-// Warp-collective forms: all 32 lanes execute them together and the lane
-// that elect.sync picks (the lowest, the same one every time) issues the
-// instruction, so the issuing loop can run warp-uniform.
+// MMA issue, warp-collective: all 32 lanes execute these together and the
+// lane that elect.sync picks (the lowest, the same one every time) issues
+// the instruction, so the issuing loop runs warp-uniform; a commit then
+// covers every MMA issued before it.  Each call issues a group of four MMAs
+// (kind::f16, one CTA) from one asm block, so the issuer spends no
+// instructions between them; `acc0` enables accumulation for the first MMA
+// and the later ones always accumulate.  SS: a[i], b[i] are the
+// shared-memory descriptors of MMA i; TS: a[i] are the TMEM addresses of A,
+// b[i] the shared-memory descriptors of B.
 __device__ __forceinline__ void tc_mma_ss_x4_elect(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4],
                                                    uint32_t idesc, uint32_t acc0) {
     asm volatile(
