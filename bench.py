@@ -347,16 +347,20 @@ def run_gpu(args):
 
         e2e_step()
         torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        for _ in range(reps):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        e2e_s = (time.perf_counter() - t0) / reps
+        with ClockSampler(local) as e2e_clk:
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            e2e_s = (time.perf_counter() - t0) / reps
         attn.check(attn.attn_device_status(sh), "e2e status")
         result["e2e"] = {"value": round(flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
                          "h2d_bytes_per_step": 3 * q.numel() * 2,
                          "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
                          "steps": reps, "ms_per_step": round(e2e_s * 1e3, 3),
+                         # the SM clock while these calls ran: the e2e loop comes after
+                         # seconds of forward work, later than the step's own samples
+                         "clocks": e2e_clk.summary(),
                          "api": "attn_fwd_host (C ABI): pinned host buffers, copies overlapped with the"
                                 " kernels in chunks of KV heads"}
         result["gpu_launches_e2e"] = (reps + 1) * chunks
