@@ -14,7 +14,10 @@ def to64(t):
     return t.detach().to("cpu").double().numpy()
 
 
-def assert_close(o, o_ref, lse=None, lse_ref=None, what=""):
+def assert_close(o, o_ref, lse=None, lse_ref=None, what="", elem_rel=0.0):
+    """The gates above; elem_rel > 0 widens the per-element bound to
+    MAX_ABS_O + elem_rel * |o_ref| (for inputs outside the configurations,
+    where |O| can approach the largest |V|)."""
     o = np.asarray(o, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     assert o.shape == o_ref.shape, (o.shape, o_ref.shape)
@@ -23,7 +26,7 @@ def assert_close(o, o_ref, lse=None, lse_ref=None, what=""):
     nref = np.linalg.norm(o_ref)
     rel = np.linalg.norm(o - o_ref) / nref if nref > 0 else np.linalg.norm(o - o_ref)
     msg = f"{what}: max|dO| {err.max():.3e} rel {rel:.3e}"
-    assert err.max() <= MAX_ABS_O, msg
+    assert np.all(err <= MAX_ABS_O + elem_rel * np.abs(o_ref)), msg
     assert rel <= REL_L2_O, msg
     if lse is not None:
         lse = np.asarray(lse, dtype=np.float64)

@@ -88,6 +88,22 @@ def test_small_shapes_match_the_oracle(attn, B, Hq, Hkv, N, d, causal):
     assert_grad_close(to64(dv), rv, "dv " + what)
 
 
+@pytest.mark.parametrize("scale", [1.0, 0.02])
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_other_scales_match_the_oracle(attn, scale, d, causal):
+    """Scales far from 1/sqrt(d): peaked rows (1.0) and nearly uniform ones (0.02)."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N = 1, 4, 2, 300
+    q, k, v = prefill_inputs(23, B, Hq, Hkv, N, d, dev)
+    dout = output_grad(23, B, Hq, N, d, dev)
+    dq, dk, dv = _fwd_bwd(attn, q, k, v, dout, causal, scale=scale)
+    rq, rk, rv = oracle.attention_bwd(to64(q), to64(k), to64(v), to64(dout), scale, causal)
+    what = f"scale {scale}, d {d}, causal {causal}"
+    assert_grad_close(to64(dq), rq, "dq " + what)
+    assert_grad_close(to64(dk), rk, "dk " + what)
+    assert_grad_close(to64(dv), rv, "dv " + what)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_tile_orders_are_bit_identical(attn, causal):
     dev = torch.device("cuda")

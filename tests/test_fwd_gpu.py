@@ -74,6 +74,27 @@ def test_forward_matches_oracle(attn, B, Hq, Hkv, N, d, causal):
     assert_close(to64(o), o_ref, to64(lse), lse_ref, what=f"{(B, Hq, Hkv, N, d, causal)}")
 
 
+@pytest.mark.parametrize("scale", [1.0, 0.02])
+@pytest.mark.parametrize("d,causal", [(128, False), (128, True), (64, True), (56, False)])
+def test_forward_other_scales(attn, scale, d, causal):
+    """Scales far from 1/sqrt(d).  At 1.0 the scaled scores of N(0, 1) inputs
+    spread over tens of units, so each row's P is peaked and its exponentials
+    against the kept reference maximum span a wide range; at 0.02 every row is
+    close to uniform."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N = 1, 4, 2, 700
+    q, k, v = prefill_inputs(11, B, Hq, Hkv, N, d, dev)
+    o, lse = _run(attn, q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), scale, causal)
+    # A peaked row's O is close to one row of V, up to about 4 in magnitude,
+    # where rounding O to bf16 alone costs up to 2^-8 |O| and rounding P to
+    # bf16 up to 2^-9 of the attended values: each element is held to the
+    # configurations' 2e-2 plus 2^-7 |O_ref|; the relative L2 and lse gates
+    # are the configurations' own.
+    assert_close(to64(o), o_ref, to64(lse), lse_ref, what=f"scale {scale}, d {d}, causal {causal}",
+                 elem_rel=2.0 ** -7)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_tile_orders_are_bit_identical_and_correct(attn, causal):
     """More units than SMs, so persistent CTAs run several units each."""
