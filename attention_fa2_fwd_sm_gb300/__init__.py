@@ -53,6 +53,7 @@ SIGNATURES = {
     "attn_fwd_host_trace_read": (_LL, [_FP, _LL]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_bwd_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "attn_bwd_workspace_bytes_ex": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _SZ, _P]),
     "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
     "attn_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
@@ -204,6 +205,10 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
 
 def attn_bwd_workspace_bytes(B, Hq, N) -> int:
     return int(lib().attn_bwd_workspace_bytes(B, Hq, N))
+
+
+def attn_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, causal) -> int:
+    return int(lib().attn_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, int(bool(causal))))
 
 
 def attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, d, scale, num_splits, max_seqlen,
@@ -374,9 +379,11 @@ def backward(q, k, v, o, lse, dout, causal=False, scale=None, tile_order=ORDER_H
     Hkv = k.shape[1]
     if scale is None:
         scale = d ** -0.5
-    nbytes = attn_bwd_workspace_bytes(B, Hq, N)
+    nbytes = attn_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, causal)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    else:
+        nbytes = min(nbytes, workspace.numel() * workspace.element_size())
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     check(attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, tile_order,
                    workspace, nbytes, stream), "attn_bwd")

@@ -358,6 +358,13 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int N) {
     return (size_t)B * Hq * (size_t)((N + 127) / 128) * 128 * 2 * sizeof(float);
 }
 
+size_t attn_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, int causal) {
+    if (validate_fwd_sizes(B, Hq, Hkv, N, d, 1.f, kHeadFirst) != ATTN_OK) return 0;
+    const size_t base = attn_bwd_workspace_bytes(B, Hq, N);
+    const size_t part = bwd_part_bytes(B, Hkv, N, d, bwd_kv_split(B, Hq, Hkv, N, causal));
+    return part ? (base + 255) / 256 * 256 + part : base;
+}
+
 int attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout, const float *lse,
              void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d, float scale, int causal,
              int tile_order, void *workspace, size_t workspace_bytes, attn_stream_t stream) {
@@ -368,6 +375,10 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
     if (tile_order < kHeadFirst || tile_order > kNaiveHeadFirst) return ATTN_ERR_ARG;
     const size_t need = (size_t)B * Hq * (size_t)((N + 127) / 128) * 128 * 2 * sizeof(float);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    // The dK/dV pass's query-head split, when the workspace also holds its partials.
+    const int kv_split = bwd_kv_split(B, Hq, Hkv, N, causal);
+    const size_t part_at = (need + 255) / 256 * 256;
+    const size_t part_bytes = bwd_part_bytes(B, Hkv, N, d, kv_split);
     const int sms = current_num_sms();
     if (sms <= 0) return note_cuda_error(cudaErrorNoDevice, "device query");
     BwdLaunch a;
@@ -389,6 +400,10 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
     a.causal = causal ? 1 : 0;
     a.order = tile_order;
     a.workspace = static_cast<float *>(workspace);
+    if (part_bytes > 0 && workspace_bytes >= part_at + part_bytes) {
+        a.kv_split = kv_split;
+        a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + part_at);
+    }
     a.wait_ns = (unsigned long long)g_wait_ns.load();
     a.num_sms = sms;
     return bwd_launch(a, reinterpret_cast<cudaStream_t>(stream));

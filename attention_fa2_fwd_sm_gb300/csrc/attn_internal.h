@@ -33,9 +33,13 @@ struct BwdLaunch {
     float scale;
     int causal, order;
     float *workspace;  // 2 * B * Hq * roundup(N, 128) floats
+    int kv_split = 1;      // dK/dV query-head split (bwd_kv_split), used when part is set
+    float *part = nullptr;  // its fp32 partials, bwd_part_bytes
     unsigned long long wait_ns;
     int num_sms;
 };
+int bwd_kv_split(int B, int Hq, int Hkv, int N, int causal);
+size_t bwd_part_bytes(int B, int Hkv, int N, int d, int kv_split);
 
 struct DecodeLaunch {
     const void *q, *kcache, *vcache;

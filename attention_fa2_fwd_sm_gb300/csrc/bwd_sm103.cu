@@ -30,6 +30,16 @@
 // five) but needs no atomic accumulation: every output element is written
 // once, by one CTA, and the result does not depend on the schedule.
 //
+// Query-head split of the dK/dV pass (non-causal GQA with few units).  A dK/dV unit
+// streams every query head of its KV head, so GQA has G times fewer, G
+// times longer units than MHA of the same work; GQA 64/8 at 8K keys has
+// 512, 3.4 waves on 152 SMs, and the last wave runs a third full.  With a
+// workspace large enough, the pass then runs as if each KV head were s
+// "virtual" KV heads of G / s query heads (the orders, windows and host maps
+// unchanged, over B * Hkv * s pairs), each unit writing fp32 partial dK and
+// dV of its query heads; dkdv_reduce_kernel sums the s partials in a fixed
+// order.  The result is deterministic and the same for every tile order.
+//
 // Both main kernels are persistent (one CTA per SM) and take units from an
 // atomic counter in the chosen order.  Head-first keeps the CTAs that run at
 // the same time on one Attention Compute Cluster, so the operand they all
@@ -108,6 +118,11 @@ struct Params {
     const float *delta;          // [B*Hq, npad]  rowsum(dO * O), 0 past N
     int B, N, npad, Hq, Hkv, G, d_store, causal, order, nblk;
     int kv_window;  // dkdv head-first: (batch, KV head) pairs interleaved per window
+    // dkdv query-head split: Hkv and G above are the virtual KV heads (Hkv *
+    // kv_split) and their query heads (G / kv_split); K and V come from real
+    // KV head g / kv_split of hkv_real, and the partials go to part.
+    int kv_split, hkv_real;
+    float *part;  // [2][B * Hkv][N][d_store] fp32: dK (scaled), then dV
     long long total_units;
     float scale, scale_log2;
     unsigned long long wait_ns;
@@ -256,6 +271,59 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 }
 
 
+// store_half_row in fp32 (the split dK/dV pass's partials).
+template <int D>
+__device__ __forceinline__ void store_half_row_f32(uint32_t t_row, int half, float *dst, bool row_ok, int d_store,
+                                                   float mul) {
+#pragma unroll
+    for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = half * (D / 64) + cc;  // 32-column chunk
+        uint32_t v[32];
+        tmem_ld32(t_row + c * 32, v);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const int col = c * 32 + g * 4;
+                if (col < d_store)
+                    *reinterpret_cast<float4 *>(dst + col) =
+                        make_float4(__uint_as_float(v[4 * g]) * mul, __uint_as_float(v[4 * g + 1]) * mul,
+                                    __uint_as_float(v[4 * g + 2]) * mul, __uint_as_float(v[4 * g + 3]) * mul);
+            }
+        }
+    }
+}
+
+// dK and dV from the split pass's partials: for each real KV head, the sum of
+// its kv_split virtual heads' fp32 partials in order g = 0, 1, ..., rounded
+// to bf16.  Virtual head g of real KV head kvh is plane (b Hkv + kvh)
+// kv_split + g; the dV partials follow all the dK partials.  One thread per
+// 4 consecutive elements of a key row (d_store is 56, 64 or 128).
+__global__ void dkdv_reduce_kernel(const float *part, __nv_bfloat16 *dk, __nv_bfloat16 *dv, int bh_real, int N,
+                                   int d_store, int kv_split) {
+    const int per_row = d_store / 4;
+    const long long rows = (long long)bh_real * N;
+    const long long n = rows * per_row;
+    const size_t plane = (size_t)rows * kv_split * d_store;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long row = i / per_row;  // (b * Hkv + kvh) * N + key
+        const int col = int(i % per_row) * 4;
+        const long long bh = row / N, key = row % N;
+        float4 sk = make_float4(0.f, 0.f, 0.f, 0.f), sv = sk;
+        for (int g = 0; g < kv_split; ++g) {
+            const size_t at = ((size_t)(bh * kv_split + g) * N + key) * d_store + col;
+            const float4 a = *reinterpret_cast<const float4 *>(part + at);
+            const float4 b = *reinterpret_cast<const float4 *>(part + plane + at);
+            sk.x += a.x; sk.y += a.y; sk.z += a.z; sk.w += a.w;
+            sv.x += b.x; sv.y += b.y; sv.z += b.z; sv.w += b.w;
+        }
+        const size_t o = (size_t)row * d_store + col;
+        *reinterpret_cast<uint2 *>(dk + o) = make_uint2(pack_bf16x2(sk.x, sk.y), pack_bf16x2(sk.z, sk.w));
+        *reinterpret_cast<uint2 *>(dv + o) = make_uint2(pack_bf16x2(sv.x, sv.y), pack_bf16x2(sv.z, sv.w));
+    }
+}
+
 // ------------------------------------------------------------------- dK, dV
 
 template <int D>
@@ -282,7 +350,9 @@ struct KvCfg {
 // Query blocks per query head that key block j meets (causal: i >= j).
 __device__ __forceinline__ int kv_first_i(const Params &p, int j) { return p.causal ? j : 0; }
 
-template <int D>
+// kPart: the split form, writing fp32 partials of virtual KV heads (see the
+// file's header); a separate instantiation, so the plain one is unchanged.
+template <int D, bool kPart>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -371,11 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(bar(C::kBarKVFull), 2 * C::kTileBytes);
+                const int kv_plane = kPart ? w.b * p.hkv_real + w.g / p.kv_split : w.b * p.Hkv + w.g;
                 for (int c = 0; c < C::kChunks; ++c) {
                     tma_load_3d(smem_u32(sK + c * C::kChunkBytes), &tmK, bar(C::kBarKVFull), c * 64,
-                                w.j * kRows, w.b * p.Hkv + w.g);
+                                w.j * kRows, kv_plane);
                     tma_load_3d(smem_u32(sV + c * C::kChunkBytes), &tmV, bar(C::kBarKVFull), c * 64,
-                                w.j * kRows, w.b * p.Hkv + w.g);
+                                w.j * kRows, kv_plane);
                 }
                 ++kv_loads;
                 const int i0 = kv_first_i(p, w.j);
@@ -641,8 +712,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key = w.j * kRows + r;
             const bool row_ok = key < p.N;
             const size_t off = ((size_t)(w.b * p.Hkv + w.g) * p.N + (row_ok ? key : 0)) * p.d_store;
-            store_half_row<D>(tmem_base + lane_off + C::kColDV, half, p.out1 + off, row_ok, p.d_store, 1.f);
-            store_half_row<D>(tmem_base + lane_off + C::kColDK, half, p.out0 + off, row_ok, p.d_store, p.scale);
+            if constexpr (kPart) {
+                const size_t plane = (size_t)p.B * p.Hkv * p.N * p.d_store;  // one of dK, dV
+                store_half_row_f32<D>(tmem_base + lane_off + C::kColDK, half, p.part + off, row_ok, p.d_store,
+                                      p.scale);
+                store_half_row_f32<D>(tmem_base + lane_off + C::kColDV, half, p.part + plane + off, row_ok,
+                                      p.d_store, 1.f);
+            } else {
+                store_half_row<D>(tmem_base + lane_off + C::kColDV, half, p.out1 + off, row_ok, p.d_store, 1.f);
+                store_half_row<D>(tmem_base + lane_off + C::kColDK, half, p.out0 + off, row_ok, p.d_store,
+                                  p.scale);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarAccEmpty));
@@ -1152,15 +1232,20 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
     if (dev < 0 || !attr_set[dev]) {
         // The setmaxnreg split assumes the launch register count; refuse a
         // build that differs (its setmaxnreg.inc could never complete).
-        cudaFuncAttributes fa, fb;
-        cudaError_t e = cudaFuncGetAttributes(&fa, dkdv_kernel<D>);
+        cudaFuncAttributes fa, fs, fb;
+        cudaError_t e = cudaFuncGetAttributes(&fa, dkdv_kernel<D, false>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fs, dkdv_kernel<D, true>);
         if (e == cudaSuccess) e = cudaFuncGetAttributes(&fb, dq_kernel<D>);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncGetAttributes(backward kernels)");
-        if (fa.numRegs != kLaunchRegs || fb.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads ||
-            fb.maxThreadsPerBlock < kThreads)
+        if (fa.numRegs != kLaunchRegs || fs.numRegs != kLaunchRegs || fb.numRegs != kLaunchRegs ||
+            fa.maxThreadsPerBlock < kThreads || fs.maxThreadsPerBlock < kThreads || fb.maxThreadsPerBlock < kThreads)
             return note_cuda_error(cudaErrorInvalidConfiguration,
                                    "backward kernel register count differs from the setmaxnreg split");
-        e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CA::kSmemBytes);
+        e = cudaFuncSetAttribute(dkdv_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 CA::kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(dkdv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     CA::kSmemBytes);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CB::kSmemBytes);
         if (e != cudaSuccess) return note_cuda_error(e, "cudaFuncSetAttribute(backward kernels)");
@@ -1185,22 +1270,49 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
     // list-scheduling simulation of the persistent CTAs (152 SMs, unit time =
     // query blocks + 1) gives GQA 64/8 causal 8K 0.78 -> 0.94 of perfect
     // balance and 16K 0.93 -> 0.98; long sequences keep one pair per window.
-    p.kv_window = dkdv_window(a.order, a.causal, a.B, a.Hkv, nblk, a.num_sms);
+    p.kv_split = 1;
+    p.hkv_real = a.Hkv;
+    p.part = nullptr;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.wait_ns = a.wait_ns;
     p.sched_slot = int(g_bwd_launch_seq.fetch_add(1) % kBwdSchedSlots);
 
-    // dK, dV
+    // dK, dV (split: over B * Hkv * kv_split virtual KV heads of G / kv_split
+    // query heads each, then the partials' sum)
+    const bool split = a.kv_split > 1 && a.part;
+    if (split) {
+        p.Hkv = a.Hkv * a.kv_split;
+        p.G = (a.Hq / a.Hkv) / a.kv_split;
+        p.kv_split = a.kv_split;
+        p.part = a.part;
+    }
+    p.kv_window = dkdv_window(a.order, a.causal, a.B, p.Hkv, nblk, a.num_sms);
     p.out0 = reinterpret_cast<__nv_bfloat16 *>(a.dk);
     p.out1 = reinterpret_cast<__nv_bfloat16 *>(a.dv);
-    p.total_units = (long long)a.B * a.Hkv * nblk;
+    p.total_units = (long long)a.B * p.Hkv * nblk;
     long long grid = p.total_units;
     if (a.order != kNaiveHeadFirst && grid > a.num_sms) grid = a.num_sms;
     if (grid > 0x7fffffffLL) return -2;
-    dkdv_kernel<D><<<unsigned(grid), kThreads, CA::kSmemBytes, stream>>>(mq, mdo, mk, mv, p);
+    if (split)
+        dkdv_kernel<D, true><<<unsigned(grid), kThreads, CA::kSmemBytes, stream>>>(mq, mdo, mk, mv, p);
+    else
+        dkdv_kernel<D, false><<<unsigned(grid), kThreads, CA::kSmemBytes, stream>>>(mq, mdo, mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return note_cuda_error(e, "dkdv_kernel launch");
+    if (split) {
+        const long long n = (long long)a.B * a.Hkv * a.N * (a.d / 4);
+        long long blocks = (n + 255) / 256;
+        const long long cap = (long long)a.num_sms * 16;
+        if (blocks > cap) blocks = cap;
+        dkdv_reduce_kernel<<<unsigned(blocks), 256, 0, stream>>>(a.part, reinterpret_cast<__nv_bfloat16 *>(a.dk),
+                                                                reinterpret_cast<__nv_bfloat16 *>(a.dv),
+                                                                a.B * a.Hkv, a.N, a.d, a.kv_split);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return note_cuda_error(e, "dkdv_reduce_kernel launch");
+        p.Hkv = a.Hkv;  // the dQ pass uses the real heads
+        p.G = a.Hq / a.Hkv;
+    }
 
     // dQ
     p.out0 = reinterpret_cast<__nv_bfloat16 *>(a.dq);
@@ -1215,6 +1327,28 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
 }
 
 }  // namespace bwd
+
+// The dK/dV pass's query-head split for a problem: the smallest s dividing
+// G = Hq / Hkv that gives at least kSplitUnits units (six waves on 152 SMs),
+// else G; 1 when the problem already has that many units, and 1 when causal:
+// there the head-first windows already balance the unequal units, and the
+// split measured 2% slower (GQA 64/8 causal 8K), its partials and their sum
+// costing more than the tail it shortens.
+int bwd_kv_split(int B, int Hq, int Hkv, int N, int causal) {
+    constexpr long long kSplitUnits = 6 * 152;
+    if (causal) return 1;
+    const int G = Hq / Hkv;
+    const long long units = (long long)B * Hkv * ((N + bwd::kRows - 1) / bwd::kRows);
+    if (units >= kSplitUnits) return 1;
+    for (int s = 2; s < G; ++s)
+        if (G % s == 0 && units * s >= kSplitUnits) return s;
+    return G;
+}
+
+size_t bwd_part_bytes(int B, int Hkv, int N, int d, int kv_split) {
+    if (kv_split <= 1) return 0;
+    return 2 * (size_t)B * Hkv * kv_split * (size_t)N * d * sizeof(float);
+}
 
 int bwd_launch(const BwdLaunch &a, cudaStream_t stream) {
     if (a.d <= 64) return bwd::launch<64>(a, stream);

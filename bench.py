@@ -747,7 +747,7 @@ def run_bwd_one(args):
     dout = output_grad(13, B, Hq, N, d, dev)
     o, lse = attn.forward(q, k, v, causal=causal, scale=d ** -0.5)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    nbytes = attn.attn_bwd_workspace_bytes(B, Hq, N)
+    nbytes = attn.attn_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, causal)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     oid = attn.ORDERS[args.order]
     fn = lambda: attn.check(attn.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, d ** -0.5,
@@ -921,7 +921,7 @@ def run_bwd_sweep(args):
         dout = output_grad(15, B, Hq, N, d, dev)
         o, lse = attn.forward(q, k, v, causal=causal, scale=d ** -0.5)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        nbytes = attn.attn_bwd_workspace_bytes(B, Hq, N)
+        nbytes = attn.attn_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, causal)
         ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         flops = bwd_flops(B, Hq, N, d, causal)
         out = {"mode": "bwd-sweep", "config": name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,

@@ -246,6 +246,14 @@ long long attn_fwd_host_trace_read(float *ms, long long capacity);
  *   NAIVE_HEAD_FIRST (the die-split order is forward-only).
  *   workspace: device memory of at least attn_bwd_workspace_bytes(B, Hq, N)
  *   bytes, 16-byte aligned; it receives -lse * log2(e) and Delta per query row.
+ *   With at least attn_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, causal) bytes
+ *   the dK/dV pass may split each KV head's query heads into s groups (non-
+ *   causal grouped-query problems with fewer than 912 dK/dV units, six waves
+ *   on 152 SMs):
+ *   each group's units write fp32 partial dK and dV into the workspace and a
+ *   fourth kernel sums the s partials in a fixed order.  The split depends
+ *   only on B, Hq, Hkv and N; its results differ from the unsplit pass's by
+ *   fp32 rounding and are, like them, independent of the tile order.
  * Three kernels run on `stream`: the Delta pre-pass, the dK/dV pass (units of
  * 128 keys of one KV head) and the dQ pass (units of 256 query rows of one
  * query head); the two main passes are persistent grids that take units in
@@ -262,6 +270,12 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const v
 
 /* Workspace bytes attn_bwd needs: 8 * B * Hq * roundup(N, 128) (0 for bad sizes). */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int N);
+
+/* Workspace bytes for attn_bwd with the dK/dV query-head split where it
+ * applies: attn_bwd_workspace_bytes(B, Hq, N) rounded up to 256, plus
+ * 8 * B * Hkv * s * N * d for s > 1 (s as attn_bwd chooses it); equal to
+ * attn_bwd_workspace_bytes when the problem is not split; 0 for bad sizes. */
+size_t attn_bwd_workspace_bytes_ex(int B, int Hq, int Hkv, int N, int d, int causal);
 
 /*
  * Split-KV grouped-query decode, one query row per (batch, query head).

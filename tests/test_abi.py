@@ -234,6 +234,17 @@ def test_backward_workspace_size(L):
     assert attn.attn_bwd_workspace_bytes(1, 2, 256) == 2 * 2 * 256 * 4
     assert attn.attn_bwd_workspace_bytes(2, 3, 129) == 2 * 2 * 3 * 256 * 4  # rows padded to 128
     assert attn.attn_bwd_workspace_bytes(0, 2, 256) == 0
+    # the dK/dV query-head split: the smallest s dividing G with >= 912 units, else G
+    base = attn.attn_bwd_workspace_bytes(1, 64, 8192)
+    assert attn.attn_bwd_workspace_bytes_ex(1, 128, 128, 8192, 128, 0) == attn.attn_bwd_workspace_bytes(1, 128, 8192)
+    assert attn.attn_bwd_workspace_bytes_ex(1, 64, 8, 32768, 128, 0) == attn.attn_bwd_workspace_bytes(1, 64, 32768)
+    # GQA 64/8 at 8K: 8 * 64 = 512 units, s = 2 gives 1024; causal never splits
+    assert attn.attn_bwd_workspace_bytes_ex(1, 64, 8, 8192, 128, 0) == (base + 255) // 256 * 256 + 8 * 8 * 2 * 8192 * 128
+    assert attn.attn_bwd_workspace_bytes_ex(1, 64, 8, 8192, 128, 1) == base
+    # 2 KV heads of 3 blocks (6 units), G = 3: no divisor reaches 912, s = G
+    base = attn.attn_bwd_workspace_bytes(1, 6, 300)
+    assert attn.attn_bwd_workspace_bytes_ex(1, 6, 2, 300, 56, 0) == (base + 255) // 256 * 256 + 8 * 2 * 3 * 300 * 56
+    assert attn.attn_bwd_workspace_bytes_ex(1, 6, 4, 300, 56, 0) == 0  # Hq % Hkv != 0
 
 
 def _dvl(**kw):

@@ -88,6 +88,40 @@ def test_small_shapes_match_the_oracle(attn, B, Hq, Hkv, N, d, causal):
     assert_grad_close(to64(dv), rv, "dv " + what)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,N,d", [(1, 8, 2, 700, 128), (2, 16, 2, 300, 64), (1, 6, 2, 257, 56)])
+def test_query_head_split_of_the_dkdv_pass(attn, B, Hq, Hkv, N, d):
+    """Non-causal grouped-query problems with few dK/dV units split each KV
+    head's query heads when the workspace holds the partials (causal ones
+    never do): the split and the unsplit
+    pass (the minimum workspace) both match the oracle, agree within fp32
+    rounding on dK and dV, and give the same dQ bit for bit."""
+    dev = torch.device("cuda")
+    causal = False
+    q, k, v = prefill_inputs(24, B, Hq, Hkv, N, d, dev)
+    dout = output_grad(24, B, Hq, N, d, dev)
+    scale = scale_of(d)
+    o, lse = attn.forward(q, k, v, causal=causal, scale=scale)
+    base = attn.attn_bwd_workspace_bytes(B, Hq, N)
+    ex = attn.attn_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, causal)
+    assert ex > base, "this shape is split"
+    assert attn.attn_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, True) == base, "causal never splits"
+    rq, rk, rv = oracle.attention_bwd(to64(q), to64(k), to64(v), to64(dout), scale, causal)
+    got = {}
+    for name, nbytes in (("split", ex), ("unsplit", base)):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        grads = attn.backward(q, k, v, o, lse, dout, causal=causal, scale=scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert attn.attn_device_status() == attn.ATTN_OK
+        what = f"{name} {(B, Hq, Hkv, N, d, causal)}"
+        for g, r, nm in zip(grads, (rq, rk, rv), ("dq", "dk", "dv")):
+            assert_grad_close(to64(g), r, nm + " " + what)
+        got[name] = grads
+    assert torch.equal(got["split"][0], got["unsplit"][0]), "dQ does not depend on the dK/dV split"
+    for a, b in zip(got["split"][1:], got["unsplit"][1:]):
+        diff = (a.float() - b.float()).abs().max().item()
+        assert diff <= 2e-2 * max(b.float().abs().max().item(), 1e-3), diff
+
+
 @pytest.mark.parametrize("scale", [1.0, 0.02])
 @pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
 def test_other_scales_match_the_oracle(attn, scale, d, causal):
@@ -155,16 +189,16 @@ def test_concurrent_launches_of_both_head_dims(attn):
         data[d] = (q, k, v, o, lse, dout)
     ref = {d: attn.backward(*data[d], causal=True) for d in data}
     torch.cuda.synchronize()
-    nbytes = attn.attn_bwd_workspace_bytes(B, H, N)
+    nbytes = {d: attn.attn_bwd_workspace_bytes_ex(B, H, H, N, d, True) for d in data}
     streams = {d: torch.cuda.Stream() for d in data}
     runs = []
     for _ in range(6):
         for d in data:
             q, k, v, o, lse, dout = data[d]
-            ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            ws = torch.empty(nbytes[d], dtype=torch.uint8, device=dev)
             grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
             attn.check(attn.attn_bwd(q, k, v, o, dout, lse, *grads, B, H, H, N, d, d ** -0.5, True, 0, ws,
-                                     nbytes, streams[d].cuda_stream), "attn_bwd")
+                                     nbytes[d], streams[d].cuda_stream), "attn_bwd")
             runs.append((d, grads, ws))
     torch.cuda.synchronize()
     attn.check(attn.attn_device_status(), "device status")
