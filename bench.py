@@ -930,7 +930,8 @@ def run_bwd_sweep(args):
             oid = attn.ORDERS[oname]
             fn = lambda: attn.check(attn.attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, d ** -0.5,
                                                   causal, oid, ws, nbytes, stream.cuda_stream), "bwd")
-            fn()
+            for _ in range(max(1, args.warmup)):
+                fn()
             ms = _time_calls(torch, fn, args.steps, None, stream)
             tf = flops / (ms / 1e3) / 1e12
             out[oname] = {"ms": round(ms, 3), "tflops": round(tf, 1), "frac": round(tf / peaks["bf16_tflops"], 4)}
