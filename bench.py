@@ -759,7 +759,9 @@ def run_bwd_one(args):
     print(json.dumps({"mode": "bwd-one", "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "causal": causal,
                       "order": args.order, "ms": round(ms, 4), "tflops": round(tf, 1),
                       "frac": round(tf / peaks["bf16_tflops"], 4),
-                      "launches_per_call": 3, "calls": args.warmup + args.steps}), flush=True)
+                      # pre-pass, dK/dV, dQ; plus the partials' sum when the dK/dV pass splits
+                      "launches_per_call": 3 + int(nbytes > attn.attn_bwd_workspace_bytes(B, Hq, N)),
+                      "calls": args.warmup + args.steps}), flush=True)
 
 
 def run_decode_one(args):
