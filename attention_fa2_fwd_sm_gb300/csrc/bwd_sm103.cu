@@ -103,14 +103,19 @@ constexpr int kThreads = 384;  // 12 warps: 4 control, 8 elementwise
 constexpr int kEwWarps = 8;    // two per TMEM lane quarter, each on half of the columns
 constexpr int kTmemCols = 512;
 // Register split after set-up (as in the forward kernel): the launch gives
-// 168 registers per thread; the control warpgroup drops to 128 (the issuers'
-// state) and the two elementwise warpgroups rise to 184
-// (128 x 128 + 256 x 184 <= 384 x 168).  The host refuses a build whose
-// launch register count differs.
+// 168 registers per thread (384 x 168 = 64512); the control warpgroup drops
+// to kCtrl (the issue loops' state) and the two elementwise warpgroups rise
+// to kEw.  The host refuses a build whose launch register count differs.
+// d = 128: 136 / 184.  d <= 64: 120 / 192, which cuts the elementwise warps'
+// spills from about 100 to 4 bytes in dK/dV and ran the backward 2.4% faster
+// at d = 64 and d = 56 (at d = 128 it measured 0.5% slower).
 constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 136;
-constexpr int kEwRegs = 184;
-static_assert(128 * kCtrlRegs + 256 * kEwRegs <= kThreads * kLaunchRegs, "register split");
+template <int D>
+struct BwdRegs {
+    static constexpr int kCtrl = D <= 64 ? 120 : 136;
+    static constexpr int kEw = D <= 64 ? 192 : 184;
+    static_assert(128 * kCtrl + 256 * kEw <= kThreads * kLaunchRegs, "register split");
+};
 
 struct Params {
     __nv_bfloat16 *out0, *out1;  // dkdv: dK, dV; dq: dQ (out1 unused)
@@ -416,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *status = &g_bwd_status;
 
     if (warp < 4) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BwdRegs<D>::kCtrl));
       if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
@@ -595,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEwRegs));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BwdRegs<D>::kEw));
         // ---------------------------------------------------------------- elementwise / epilogue
         // Warpgroup h = (w - 4) / 4 owns half-buffer h: query rows [64 h, +64)
         // of every block; warp w reads TMEM lanes [32 (w % 4), +32), one key
@@ -899,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *status = &g_bwd_status;
 
     if (warp < 4) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BwdRegs<D>::kCtrl));
       if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
@@ -1077,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEwRegs));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BwdRegs<D>::kEw));
         // ---------------------------------------------------------------- elementwise / epilogue
         // Warpgroup t = (w - 4) / 4 owns tile t; warp w reads TMEM lanes
         // [32 (w % 4), +32), one query row per thread.
