@@ -136,41 +136,51 @@ struct Params {
 
 // ------------------------------------------------------------------ pre-pass
 
-// One warp per padded query row: Delta = sum_c dO[c] * O[c] (fp32) and
-// -lse * log2(e) (negated, so the exponent argument is one FMA); rows at or
-// past N get -inf and 0.
+// Delta = sum_c dO[c] * O[c] (fp32) and -lse * log2(e) (negated, so the
+// exponent argument is one FMA) per padded query row; rows at or past N get
+// -inf and 0.  Eight lanes share a row, each reading 16-byte pieces of O and
+// dO (a row of d bf16 is d / 8 pieces: 7, 8 or 16), so a warp covers four
+// rows at a time.  (One warp per row with 4-byte loads ran at under half of
+// the HBM bandwidth.)
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ dout,
                                                       const float *__restrict__ lse, float *nlse2,
                                                       float *delta, int N, int npad, int d,
                                                       long long rows) {
     const int lane = threadIdx.x & 31;
+    const int l8 = lane & 7;        // lane within the row's group of eight
+    const int pieces = d / 8;       // 16-byte pieces per row
+    const long long groups = (rows + 3) / 4;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-         r += warps) {
-        const long long bh = r / npad;
-        const int n = int(r % npad);
-        if (n >= N) {
-            if (lane == 0) {
-                nlse2[r] = -INFINITY;
-                delta[r] = 0.f;
-            }
-            continue;
-        }
-        const size_t base = ((size_t)bh * N + n) * d;
+    for (long long gi = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gi < groups;
+         gi += warps) {
+        const long long r = gi * 4 + (lane >> 3);
+        const bool valid = r < rows;
+        const long long bh = valid ? r / npad : 0;
+        const int n = valid ? int(r % npad) : 0;
+        const bool live = valid && n < N;
         float acc = 0.f;
-        for (int c = 2 * lane; c < d; c += 64) {
-            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o + base + c);
-            const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162 *>(dout + base + c);
-            const float2 af = __bfloat1622float2(a), gf = __bfloat1622float2(g);
-            acc = fmaf(af.x, gf.x, acc);
-            acc = fmaf(af.y, gf.y, acc);
-        }
+        if (live) {
+            const size_t base = ((size_t)bh * N + n) * d;
+            for (int c = l8; c < pieces; c += 8) {
+                const uint4 a = *reinterpret_cast<const uint4 *>(o + base + (size_t)c * 8);
+                const uint4 g = *reinterpret_cast<const uint4 *>(dout + base + (size_t)c * 8);
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-            nlse2[r] = -(lse[(size_t)bh * N + n] * 1.4426950408889634f);
-            delta[r] = acc;
+                for (int k = 0; k < 4; ++k) {
+                    const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&aw[k]));
+                    const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gw[k]));
+                    acc = fmaf(af.x, gf.x, acc);
+                    acc = fmaf(af.y, gf.y, acc);
+                }
+            }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (valid && l8 == 0) {
+            nlse2[r] = live ? -(lse[(size_t)bh * N + n] * 1.4426950408889634f) : -INFINITY;
+            delta[r] = live ? acc : 0.f;
         }
     }
 }
@@ -1214,7 +1224,7 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
 
     // Pre-pass: Delta and lse * log2(e).
     {
-        long long blocks = (rows + 7) / 8;
+        long long blocks = (rows + 31) / 32;  // 8 warps of 4 rows
         const long long cap = (long long)a.num_sms * 16;
         if (blocks > cap) blocks = cap;
         bwd_pre_kernel<<<unsigned(blocks), 256, 0, stream>>>(
