@@ -249,15 +249,15 @@ long long attn_fwd_host_trace_read(float *ms, long long capacity);
  *   With at least attn_bwd_workspace_bytes_ex(B, Hq, Hkv, N, d, causal) bytes
  *   the dK/dV pass may split each KV head's query heads into s groups (non-
  *   causal grouped-query problems with fewer than 912 dK/dV units, six waves
- *   on 152 SMs):
- *   each group's units write fp32 partial dK and dV into the workspace and a
- *   fourth kernel sums the s partials in a fixed order.  The split depends
- *   only on B, Hq, Hkv and N; its results differ from the unsplit pass's by
- *   fp32 rounding and are, like them, independent of the tile order.
- * Three kernels run on `stream`: the Delta pre-pass, the dK/dV pass (units of
- * 128 keys of one KV head) and the dQ pass (units of 256 query rows of one
- * query head); the two main passes are persistent grids that take units in
- * the tile order.  Under HEAD_FIRST a causal dK/dV pass runs windows of the
+ *   on 152 SMs): each group's units write fp32 partial dK and dV into the
+ *   workspace and a fourth kernel sums the s partials in a fixed order.  The
+ *   split depends only on B, Hq, Hkv, N and causal; its results differ from
+ *   the unsplit pass's by fp32 rounding and are, like them, independent of
+ *   the tile order.
+ * Three kernels run on `stream` (four when the dK/dV pass splits): the Delta
+ * pre-pass, the dK/dV pass (units of 128 keys of one KV head) and the dQ pass
+ * (units of 256 query rows of one query head); the two main passes are
+ * persistent grids that take units in the tile order.  Under HEAD_FIRST a causal dK/dV pass runs windows of the
  * fewest (batch, KV head) pairs whose key blocks cover the SMs three times,
  * longest block first across the window, so that no head's long blocks start
  * at the end of the launch.  Every output element is written once; results
