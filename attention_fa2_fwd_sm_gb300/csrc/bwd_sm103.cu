@@ -108,11 +108,13 @@ constexpr int kTmemCols = 512;
 // to kEw.  The host refuses a build whose launch register count differs.
 // d = 128: 136 / 184.  d <= 64: 120 / 192, which cuts the elementwise warps'
 // spills from about 100 to 4 bytes in dK/dV and ran the backward 2.4% faster
-// at d = 64 and d = 56 (at d = 128 it measured 0.5% slower).
+// at d = 64 and d = 56 (at d = 128 it measured 0.5% slower); the d <= 64 dQ
+// kernel's control warpgroup takes 112 (its spills 24 / 76 -> 8 / 8 bytes,
+// +1.4% at d = 64).
 constexpr int kLaunchRegs = 168;
-template <int D>
+template <int D, bool kDq = false>
 struct BwdRegs {
-    static constexpr int kCtrl = D <= 64 ? 120 : 136;
+    static constexpr int kCtrl = D <= 64 ? (kDq ? 112 : 120) : 136;
     static constexpr int kEw = D <= 64 ? 192 : 184;
     static_assert(128 * kCtrl + 256 * kEw <= kThreads * kLaunchRegs, "register split");
 };
@@ -914,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *status = &g_bwd_status;
 
     if (warp < 4) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BwdRegs<D>::kCtrl));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BwdRegs<D, true>::kCtrl));
       if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
@@ -1092,7 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BwdRegs<D>::kEw));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BwdRegs<D, true>::kEw));
         // ---------------------------------------------------------------- elementwise / epilogue
         // Warpgroup t = (w - 4) / 4 owns tile t; warp w reads TMEM lanes
         // [32 (w % 4), +32), one query row per thread.
