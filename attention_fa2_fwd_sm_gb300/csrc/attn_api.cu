@@ -140,7 +140,7 @@ int attn_tile_map_die_split(int B, int Hq, int Hkv, int N, int causal, int die, 
     const int nb = unit_blocks(N);
     const long long u = die_split_unit(die, k, B, Hkv, Hq / Hkv, nb);
     if (u < 0) return ATTN_ERR_ARG;
-    const Tile t = unit_to_tile(kHeadFirst, u, Hq, Hq / Hkv, nb, causal ? 1 : 0);
+    const Tile t = unit_to_tile(kDieSplitHeadFirst, u, Hq, Hq / Hkv, nb, causal ? 1 : 0);  // head-first ids
     *b = t.b;
     *h = t.h;
     *m = t.m;

@@ -885,6 +885,9 @@ int fwd_pair_launch(const FwdLaunch &a, cudaStream_t stream) {
         const int rc = die_map_device(&p.die_of_sm);
         if (rc < 0) return rc;
     }
+    // Causal GQA head-first stays ACC by ACC at every size here (this ablation
+    // was measured that way); the one-CTA launch reduces small entries to
+    // block-first (effective_order).
     const bool grouped = grouped_causal_order(a.order, p.G, p.causal);
     auto kernel = grouped ? fwd_pair_kernel<true> : fwd_pair_kernel<false>;
 

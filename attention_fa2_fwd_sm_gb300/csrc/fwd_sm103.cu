@@ -46,7 +46,8 @@ int launch(const FwdLaunch &a, cudaStream_t stream) {
         const int rc = die_map_device(&p.die_of_sm);
         if (rc < 0) return rc;
     }
-    const bool grouped = grouped_causal_order(a.order, p.G, p.causal);
+    p.order = effective_order(a.order, a.Hq, p.G, p.nb, p.causal);  // head-first over a whole entry
+    const bool grouped = grouped_causal_order(p.order, p.G, p.causal);
     auto kernel = grouped ? fwd_kernel<D, kMapGrouped> : fwd_kernel<D, kMapOrder>;
     static bool attr_set[2][kMaxDevices] = {};  // per instantiation and device
     const int dev = slot_for_device();

@@ -15,7 +15,12 @@ Exploiting GPU Architectural NUMA Effects", section 2 Q2 and section 3
   groups, (batch, kv group, head in group, block) order is simply
   (batch, head, block).  For causal attention with several query heads per
   KV head the ACC's units go (block rank, head in group): every head's
-  longest unit, then every head's second longest, and so on.
+  longest unit, then every head's second longest, and so on -- unless the
+  batch entry's K/V all fit in L2 together (KV heads x row blocks <= 512,
+  ``WHOLE_ENTRY_BLOCKS``), where no ACC can evict another's K/V and the
+  entry's units go longest first over all its query heads, which is the
+  block-first sequence (a reading: the pages' head-first exists for that
+  cache reuse).
 * block-first: all heads of one row block before the next row block.
 * naive head-first: the head-first linear order, but each unit is its own
   CTA and the hardware decides where it runs.
@@ -40,11 +45,20 @@ def num_blocks(n: int, bm: int) -> int:
     return -(-n // bm)
 
 
-def unit_to_tile(order: int, u: int, batch: int, heads: int, nb: int, causal: bool, group: int = 1):
-    """Linear unit id -> (b, h, m); ``group`` query heads share one KV head."""
+WHOLE_ENTRY_BLOCKS = 512  # KV heads x row blocks of an entry whose K/V fit in L2 together
+
+
+def unit_to_tile(order: int, u: int, batch: int, heads: int, nb: int, causal: bool, group: int = 1,
+                 whole_entry: bool = True):
+    """Linear unit id -> (b, h, m); ``group`` query heads share one KV head.
+    ``whole_entry=False`` keeps causal GQA head-first ACC by ACC at every
+    size (the order the die-split placement deals out)."""
     total = batch * heads * nb
     if not 0 <= u < total:
         raise ValueError("unit out of range")
+    if (whole_entry and order == HEAD_FIRST and causal and group > 1
+            and (heads // group) * nb <= WHOLE_ENTRY_BLOCKS):
+        order = BLOCK_FIRST
     if order == HEAD_FIRST and causal and group > 1:
         acc, w = divmod(u, group * nb)       # ACC = (batch entry, KV head)
         r, head_in_group = divmod(w, group)  # block rank, then head

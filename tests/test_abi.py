@@ -67,7 +67,8 @@ def test_missing_library_fails_loudly(monkeypatch):
 @pytest.mark.parametrize("order", T.ORDERS)
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,H,Hkv,N", [(1, 2, 2, 256), (2, 3, 3, 300), (1, 8, 8, 4096), (3, 5, 5, 1),
-                                       (1, 8, 2, 1300), (2, 6, 3, 600), (1, 64, 8, 2048)])
+                                       (1, 8, 2, 1300), (2, 6, 3, 600), (1, 64, 8, 2048),
+                                       (1, 64, 8, 16384), (1, 64, 8, 16385), (1, 8, 2, 70000)])
 def test_scheduler_matches_the_definitions(L, order, causal, B, H, Hkv, N):
     nb = T.num_blocks(N, 256)
     assert attn.attn_fwd_units(B, H, N) == B * H * nb

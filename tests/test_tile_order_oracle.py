@@ -13,7 +13,7 @@ def test_orders_are_bijections(order, causal, B, H, nb, G):
     assert seen == {(b, h, m) for b in range(B) for h in range(H) for m in range(nb)}
 
 
-@pytest.mark.parametrize("B,Hq,G,nb", [(1, 16, 4, 5), (2, 6, 3, 4), (1, 64, 8, 32)])
+@pytest.mark.parametrize("B,Hq,G,nb", [(1, 16, 4, 130), (2, 6, 3, 257), (1, 64, 8, 65)])
 def test_causal_gqa_head_first_runs_each_acc_longest_first(B, Hq, G, nb):
     """Each ACC's G * nb units are consecutive, and inside the ACC the units
     come in non-increasing causal length (block index descending), every
@@ -141,7 +141,7 @@ def test_die_split_each_die_is_head_first_over_its_accs():
     ACCs; for one ACC per die it is exactly the head-first order of that ACC."""
     B, Hq, Hkv, nb = 1, 4, 2, 3
     G = Hq // Hkv
-    hf = [T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, True, G) for u in range(B * Hq * nb)]
+    hf = [T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, True, G, whole_entry=False) for u in range(B * Hq * nb)]
     for d in (0, 1):
         assert T.die_split_sequence(d, B, Hq, Hkv, nb, True) == [x for x in hf if x[1] // G == d]
 
@@ -150,7 +150,8 @@ def test_die_split_each_die_is_head_first_over_its_accs():
 def test_die_split_with_one_die_is_head_first(causal):
     B, Hq, Hkv, nb = 2, 6, 3, 4
     assert T.die_split_sequence(0, B, Hq, Hkv, nb, causal, dies=1) == [
-        T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, causal, Hq // Hkv) for u in range(B * Hq * nb)]
+        T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, causal, Hq // Hkv, whole_entry=False)
+        for u in range(B * Hq * nb)]
 
 
 # ------------------------------------------------------- backward dK/dV order
@@ -204,3 +205,18 @@ def test_dkdv_head_first_without_a_window_is_pair_major():
     assert seq == [(0, 0, 0), (0, 0, 1), (0, 0, 2), (0, 1, 0), (0, 1, 1), (0, 1, 2),
                    (1, 0, 0), (1, 0, 1), (1, 0, 2), (1, 1, 0), (1, 1, 1), (1, 1, 2)]
     assert T.dkdv_sequence(T.BLOCK_FIRST, 1, 2, 256, True, 152) == [(0, 0, 0), (0, 1, 0), (0, 0, 1), (0, 1, 1)]
+
+
+@pytest.mark.parametrize("B,Hq,G,nb", [(1, 16, 4, 5), (2, 6, 3, 4), (1, 64, 8, 32), (1, 64, 8, 64), (3, 8, 2, 64)])
+def test_causal_gqa_head_first_over_a_whole_entry_is_block_first(B, Hq, G, nb):
+    """When an entry's K/V fit in L2 together (KV heads x row blocks <= 512)
+    causal GQA head-first takes the block-first sequence; one block more per
+    head and it is ACC by ACC again."""
+    assert (Hq // G) * nb <= T.WHOLE_ENTRY_BLOCKS
+    for u in range(B * Hq * nb):
+        assert (T.unit_to_tile(T.HEAD_FIRST, u, B, Hq, nb, True, G)
+                == T.unit_to_tile(T.BLOCK_FIRST, u, B, Hq, nb, True, G))
+    big = T.WHOLE_ENTRY_BLOCKS // (Hq // G) + 1
+    seq = [T.unit_to_tile(T.HEAD_FIRST, u, 1, Hq, big, True, G) for u in range(Hq * big)]
+    assert {h // G for _, h, _ in seq[:G * big]} == {0}  # the first ACC's units come first
+
