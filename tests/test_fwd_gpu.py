@@ -114,6 +114,27 @@ def test_tile_orders_are_bit_identical_and_correct(attn, causal):
         assert_close(to64(o[0, h, rows]), o_ref, to64(lse[0, h, rows]), l_ref, what=f"head {h}")
 
 
+@pytest.mark.parametrize("N", [16384, 16385])
+def test_causal_gqa_head_first_on_both_sides_of_the_whole_entry_rule(attn, N):
+    """8 KV heads of 64 row blocks (16384 keys) fit in L2 together, so
+    head-first runs the block-first sequence; one more key (65 blocks) keeps
+    it ACC by ACC, in the grouped instantiation.  Both sides are bit-identical
+    to every other order and match the oracle on sampled rows."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, d = 1, 16, 8, 64
+    q, k, v = prefill_inputs(6, B, Hq, Hkv, N, d, dev)
+    outs = [_run(attn, q, k, v, True, order=o) for o in (0, 1, 2, 3)]
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+    o, lse = outs[0]
+    rows = sample_rows(N)
+    for h in sample_heads(Hq, Hkv):
+        g = h // (Hq // Hkv)
+        o_ref, l_ref = oracle.attention_rows(to64(q[0, h, rows]), to64(k[0, g]), to64(v[0, g]), scale_of(d),
+                                             True, rows)
+        assert_close(to64(o[0, h, rows]), o_ref, to64(lse[0, h, rows]), l_ref, what=f"N={N} head {h}")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_die_split_order_with_an_odd_acc_count(attn, causal):
     """Nine ACCs over two dies (one die runs out first and takes the other's
