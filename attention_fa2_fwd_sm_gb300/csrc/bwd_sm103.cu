@@ -1331,10 +1331,14 @@ int launch(const BwdLaunch &a, cudaStream_t stream) {
         p.G = a.Hq / a.Hkv;
     }
 
-    // dQ
+    // dQ.  Its units are the forward's (256 query rows), and causal GQA
+    // head-first over an entry whose K/V all fit in L2 together takes the
+    // block-first sequence, as the forward does (effective_order).
+    const int nq = (a.N + 2 * kRows - 1) / (2 * kRows);
+    p.order = effective_order(a.order, a.Hq, p.G, nq, p.causal);
     p.out0 = reinterpret_cast<__nv_bfloat16 *>(a.dq);
     p.out1 = nullptr;
-    p.total_units = (long long)a.B * a.Hq * ((a.N + 2 * kRows - 1) / (2 * kRows));  // 256-row units
+    p.total_units = (long long)a.B * a.Hq * nq;  // 256-row units
     grid = p.total_units;
     if (a.order != kNaiveHeadFirst && grid > a.num_sms) grid = a.num_sms;
     if (grid > 0x7fffffffLL) return -2;

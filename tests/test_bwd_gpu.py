@@ -151,6 +151,31 @@ def test_tile_orders_are_bit_identical(attn, causal):
             assert torch.equal(a, b), f"order {order}"
 
 
+@pytest.mark.parametrize("N", [16384, 16385])
+def test_causal_gqa_dq_order_on_both_sides_of_the_whole_entry_rule(attn, N):
+    """The dQ pass takes the forward's 256-row units: 8 KV heads of 64 such
+    blocks (16384 keys) fit in L2 together and run the block-first sequence
+    under head-first; one more key keeps the ACC-by-ACC order.  Every order
+    gives the same gradients bit for bit, and dQ matches the oracle on
+    sampled rows of sampled heads."""
+    dev = torch.device("cuda")
+    B, Hq, Hkv, d = 1, 16, 8, 64
+    G = Hq // Hkv
+    q, k, v = prefill_inputs(27, B, Hq, Hkv, N, d, dev)
+    dout = output_grad(27, B, Hq, N, d, dev)
+    got = _fwd_bwd(attn, q, k, v, dout, True, order=0)
+    for order in (1, 2):
+        other = _fwd_bwd(attn, q, k, v, dout, True, order=order)
+        for a, b in zip(other, got):
+            assert torch.equal(a, b), f"order {order}"
+    rows = sample_rows(N)
+    for h in sample_heads(Hq, Hkv):
+        g = h // G
+        rq, _, _ = oracle.attention_bwd_head(to64(q[0, h, rows]), to64(k[0, g]), to64(v[0, g]),
+                                             to64(dout[0, h, rows]), scale_of(d), True, qpos=rows)
+        assert_grad_close(to64(got[0][0, h, rows]), rq, f"dq N={N} head {h}")
+
+
 def test_causal_dkdv_windows_with_a_partial_last_window(attn):
     """Causal head-first dK/dV runs windows of (batch, KV head) pairs longest
     first, sized to cover the SMs three times.  Seven KV heads with windows of
