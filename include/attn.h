@@ -71,6 +71,10 @@ enum attn_status {
  *    Q2 and section 3 "before/after" table).  Inside an ACC the row blocks
  *    of one head follow each other; for causal GQA the ACC's units instead
  *    run longest first across its heads (block descending, then head).
+ *    Causal GQA on batch entries whose K/V all fit in L2 together (Hkv times
+ *    ceil(N / 256) at most 512) runs longest first over all the entry's
+ *    heads instead, which is BLOCK_FIRST's sequence: no ACC can then evict
+ *    another's K/V.  The backward's dQ pass (same units) follows this order.
  *  BLOCK_FIRST: all heads of one row block before the next row block (the
  *    pages' "Naive Block-first" baseline).
  *  NAIVE_HEAD_FIRST: head-first linear order, but one CTA per unit with the
@@ -257,7 +261,8 @@ long long attn_fwd_host_trace_read(float *ms, long long capacity);
  * Three kernels run on `stream` (four when the dK/dV pass splits): the Delta
  * pre-pass, the dK/dV pass (units of 128 keys of one KV head) and the dQ pass
  * (units of 256 query rows of one query head); the two main passes are
- * persistent grids that take units in the tile order.  Under HEAD_FIRST a causal dK/dV pass runs windows of the
+ * persistent grids that take units in the tile order (the dQ pass in the
+ * forward's, as attn_tile_map gives it).  Under HEAD_FIRST a causal dK/dV pass runs windows of the
  * fewest (batch, KV head) pairs whose key blocks cover the SMs three times,
  * longest block first across the window, so that no head's long blocks start
  * at the end of the launch.  Every output element is written once; results
