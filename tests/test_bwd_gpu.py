@@ -3,10 +3,13 @@
 The kernels take the GPU forward pass's own output and log-sum-exp (as a
 training step would) and the oracle computes the exact gradient from the same
 bf16 q, k, v, dO.  Small shapes are compared element by element (several
-blocks, ragged tails, N = 1, GQA, causal, d = 56/64/128); a larger shape on
-sampled rows and through identities of the softmax Jacobian.  Structural
+blocks, ragged tails, N = 1, GQA, causal, d = 56/64/128); a larger shape and
+the backward sweep's full sizes on sampled rows and through identities of the
+softmax Jacobian.  Structural
 identities are checked bit for bit: the three tile orders, and d = 56
 against explicit zero padding to 64."""
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -277,6 +280,63 @@ def test_larger_shape_sampled_rows_and_identities(attn, causal):
         assert torch.linalg.vector_norm(dk32[0, gg].sum(0)).item() <= 1e-2 * norm
         want = dout[0, gg * G:(gg + 1) * G].float().sum((0, 1))
         assert torch.allclose(dv32[0, gg].sum(0), want, rtol=1e-2, atol=1e-2 * want.abs().max().item())
+
+
+FULL_BWD = [
+    # the backward sweep's configurations: name, B, Hq, Hkv, N, d, causal
+    ("mha", 1, 128, 128, 8192, 128, False),
+    ("gqa", 1, 64, 8, 8192, 128, False),
+    ("gqa", 1, 64, 8, 8192, 128, True),
+    ("mha", 1, 128, 128, 32768, 128, False),
+    ("gqa", 1, 64, 8, 32768, 128, False),
+    ("gqa", 1, 64, 8, 32768, 128, True),
+    ("deepseek", 1, 128, 128, 32768, 56, True),
+]
+
+
+@pytest.mark.parametrize("name,B,Hq,Hkv,N,d,causal", FULL_BWD)
+def test_full_size_sampled(attn, name, B, Hq, Hkv, N, d, causal):
+    """Full sizes, in the launch configuration the sweep times (head-first,
+    the library's own workspace choice): dQ on sampled rows of sampled heads
+    against the oracle (a row of dQ needs only its own query row); on every KV
+    head the identities that hold at any size, sum_j dK_j = 0 and sum_j dV_j =
+    the group's summed dO; at 8K one KV head's dK and dV in full."""
+    dev = torch.device("cuda")
+    cfg = {"mha": 31, "gqa": 32, "deepseek": 33}[name] + (4 if causal else 0)
+    q, k, v = prefill_inputs(cfg, B, Hq, Hkv, N, d, dev)
+    dout = output_grad(cfg, B, Hq, N, d, dev)
+    scale = scale_of(d)
+    G = Hq // Hkv
+    try:
+        dq, dk, dv = _fwd_bwd(attn, q, k, v, dout, causal)
+        rows = sample_rows(N)
+        for h in sample_heads(Hq, Hkv):
+            g = h // G
+            rq, _, _ = oracle.attention_bwd_head(to64(q[0, h, rows]), to64(k[0, g]), to64(v[0, g]),
+                                                 to64(dout[0, h, rows]), scale, causal, qpos=rows)
+            assert_grad_close(to64(dq[0, h, rows]), rq, f"{name} N={N} dq head {h}")
+        dk32, dv32 = dk.float(), dv.float()
+        for gg in range(Hkv):
+            norm = torch.linalg.vector_norm(dk32[0, gg]).item()
+            assert torch.linalg.vector_norm(dk32[0, gg].sum(0)).item() <= 1e-2 * norm, f"sum dK, KV head {gg}"
+            want = dout[0, gg * G:(gg + 1) * G].float().sum((0, 1))
+            assert torch.allclose(dv32[0, gg].sum(0), want, rtol=1e-2, atol=1e-2 * want.abs().max().item()), \
+                f"sum dV, KV head {gg}"
+        if N <= 8192:
+            g = Hkv - 1
+            rk = np.zeros((N, d))
+            rv = np.zeros((N, d))
+            for h in range(g * G, (g + 1) * G):
+                _, rkh, rvh = oracle.attention_bwd_head(to64(q[0, h]), to64(k[0, g]), to64(v[0, g]),
+                                                        to64(dout[0, h]), scale, causal)
+                rk += rkh
+                rv += rvh
+            assert_grad_close(to64(dk[0, g]), rk, f"{name} N={N} dk")
+            assert_grad_close(to64(dv[0, g]), rv, f"{name} N={N} dv")
+    finally:
+        del q, k, v, dout
+        gc.collect()
+        torch.cuda.empty_cache()
 
 
 def test_single_key_gives_zero_q_and_k_gradients(attn):
