@@ -167,3 +167,33 @@ def test_host_forward_with_the_pair_scheme(attn):
     attn.check(attn.attn_device_status(), "device status")
     assert torch.equal(o.view(torch.int16), o_dev.cpu().view(torch.int16))
     assert torch.equal(lse, lse_dev.cpu())
+
+
+def test_host_forward_at_the_bench_size_is_bit_identical(attn):
+    """The end-to-end call the benchmark times: MHA B=1, H=128, N=131072,
+    d=128, non-causal, head-first, pinned host buffers and the library's
+    default chunking.  Its outputs equal attn_fwd's on the same inputs bit for
+    bit (the device result is itself compared with the oracle at this size in
+    the forward tests)."""
+    dev = torch.device("cuda")
+    B, H, N, d = 1, 128, 131072, 128
+    scale = scale_of(d)
+
+    def pinned(t):
+        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+
+    q, k, v = prefill_inputs(11, B, H, H, N, d, dev)
+    o_dev, lse_dev = attn.forward(q, k, v, causal=False, scale=scale)
+    attn.check(attn.attn_device_status(), "device status")
+    hq, hk, hv = pinned(q), pinned(k), pinned(v)
+    o_ref, lse_ref = pinned(o_dev), pinned(lse_dev)
+    del q, k, v, o_dev, lse_dev
+    torch.cuda.empty_cache()
+    try:
+        o, lse = attn.forward_host(hq, hk, hv, causal=False, scale=scale, kv_heads_per_chunk=0)
+        attn.check(attn.attn_device_status(), "device status")
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(lse, lse_ref)
+    finally:
+        del hq, hk, hv, o_ref, lse_ref
+        torch.cuda.empty_cache()
