@@ -113,3 +113,51 @@ def test_many_users_per_plan_thread(attn):
     assert head == [len(items_ref), c_ref]
     o_ref, _ = oracle.decode(to64(q), to64(kc), to64(vc), lens, d ** -0.5)
     assert_close(to64(o), o_ref, what="600 users")
+
+
+BENCH_WORKLOADS = [
+    # the ragged workloads the benchmark times (Hq=64, Hkv=8, d=128): name, s_max, seqlens
+    ("one 64K user + 15 of 2K", 65536, [65536] + [2048] * 15),
+    ("64 users uniform in [1, 16K]", 16384, None),  # lengths drawn from a seeded generator
+    ("8 users of 32K", 32768, [32768] * 8),
+]
+
+
+@pytest.mark.parametrize("name,s_max,lens", BENCH_WORKLOADS)
+def test_benchmark_workloads_every_element(attn, name, s_max, lens):
+    """Every output element of the benchmark's ragged workloads against the
+    oracle, one user at a time (only that user's keys are widened to fp64;
+    users run on a thread pool, the oracle's C calls release the interpreter
+    lock); the device work list equals the oracle's plan."""
+    import gc
+    from concurrent.futures import ThreadPoolExecutor
+    dev = torch.device("cuda")
+    Hq, Hkv, d = 64, 8, 128
+    if lens is None:
+        g = torch.Generator().manual_seed(47)
+        lens = torch.randint(1, s_max + 1, (64,), generator=g).tolist()
+    B = len(lens)
+    q, kc, vc = decode_inputs(48, B, Hq, Hkv, s_max, d, dev)
+    seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+    try:
+        o, ws = attn.decode_varlen(q, kc, vc, seq)
+        torch.cuda.synchronize()
+        assert attn.attn_device_status() == attn.ATTN_OK
+        c_ref, items_ref = oracle.varlen_plan(lens, s_max, Hkv, _target())
+        assert ws[:8].view(torch.int32).tolist() == [len(items_ref), c_ref]
+        o64, q64 = to64(o), to64(q)
+
+        def user(b):
+            n = lens[b]
+            kb = kc[b, :, :n].double().cpu().numpy()
+            vb = vc[b, :, :n].double().cpu().numpy()
+            o_ref, _ = oracle.decode(q64[b:b + 1], kb[None], vb[None], [n], d ** -0.5)
+            return b, o_ref
+
+        with ThreadPoolExecutor(max_workers=min(8, oracle.default_threads())) as pool:
+            for b, o_ref in pool.map(user, range(B)):
+                assert_close(o64[b:b + 1], o_ref, what=f"{name}: user {b}, {lens[b]} keys")
+    finally:
+        del q, kc, vc
+        gc.collect()
+        torch.cuda.empty_cache()
