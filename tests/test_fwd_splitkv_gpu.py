@@ -97,23 +97,27 @@ def test_splitkv_agrees_with_the_forward(attn):
         assert_close(to64(o2), to64(o1), to64(l2), to64(l1), what=f"split-KV ({splits}) vs attn_fwd")
 
 
-def test_splitkv_long_causal_gqa_sampled_rows(attn):
-    """The long-context case the split is for: GQA 64/8, d = 128, causal, 128K
-    keys (two 64K-key ranges by the library's rule), on sampled rows of
-    sampled heads."""
+@pytest.mark.parametrize("name,Hq,Hkv,d,causal", [("gqa", 64, 8, 128, True), ("mha", 128, 128, 128, False),
+                                                  ("deepseek", 128, 128, 56, True)])
+def test_splitkv_long_context_sampled_rows(attn, name, Hq, Hkv, d, causal):
+    """The long-context configurations the split is for and the benchmark
+    times, at 128K keys (two 64K-key ranges by the library's rule at d = 128):
+    GQA 64/8 causal, MHA 128 heads, and the DeepSeek-like d = 56 causal; on
+    sampled rows of sampled heads."""
     dev = torch.device("cuda")
-    B, Hq, Hkv, N, d = 1, 64, 8, 131072, 128
+    B, N = 1, 131072
     q, k, v = prefill_inputs(11, B, Hq, Hkv, N, d, dev)
     try:
-        assert attn.attn_fwd_splitkv_workspace_bytes(B, Hq, N, d, 0) == B * Hq * N * 2 * (d + 1) * 4
-        o, lse, ws = _run(attn, q, k, v, True, 0)
+        if d == 128:
+            assert attn.attn_fwd_splitkv_workspace_bytes(B, Hq, N, d, 0) == B * Hq * N * 2 * (d + 1) * 4
+        o, lse, ws = _run(attn, q, k, v, causal, 0)
         del ws
         for h in sample_heads(Hq, Hkv):
             g = h // (Hq // Hkv)
             rows = sample_rows(N)
             o_ref, l_ref = oracle.attention_rows(to64(q[0, h, rows]), to64(k[0, g]), to64(v[0, g]), scale_of(d),
-                                                 True, rows)
-            assert_close(to64(o[0, h, rows]), o_ref, to64(lse[0, h, rows]), l_ref, what=f"128K causal head {h}")
+                                                 causal, rows)
+            assert_close(to64(o[0, h, rows]), o_ref, to64(lse[0, h, rows]), l_ref, what=f"{name} 128K head {h}")
     finally:
         del q, k, v
         gc.collect()
