@@ -127,3 +127,28 @@ def test_pair_timeout_is_reported_and_recovered(attn):
     o, lse = _run(attn, q, k, v, True)
     o_ref, lse_ref = oracle.attention(to64(q), to64(k), to64(v), scale_of(128), True)
     assert_close(to64(o), o_ref, to64(lse), lse_ref, what="after a timeout")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,causal", [(1, 128, 128, 32768, False), (1, 64, 8, 131072, True)])
+def test_pair_full_size_equals_the_single_cta_scheme(attn, B, Hq, Hkv, N, causal):
+    """Sizes the forward sweep times with the pair scheme: bit for bit the
+    one-CTA result (the same K = 16 steps in the same order), and sampled rows
+    of sampled heads against the oracle."""
+    import gc
+    dev = torch.device("cuda")
+    d = 128
+    q, k, v = prefill_inputs(12, B, Hq, Hkv, N, d, dev)
+    try:
+        o1, l1 = _run(attn, q, k, v, causal, scheme=attn.FWD_SINGLE_CTA)
+        o2, l2 = _run(attn, q, k, v, causal, scheme=attn.FWD_CTA_PAIR)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+        rows = sample_rows(N)
+        for h in sample_heads(Hq, Hkv):
+            g = h // (Hq // Hkv)
+            o_ref, l_ref = oracle.attention_rows(to64(q[0, h, rows]), to64(k[0, g]), to64(v[0, g]), scale_of(d),
+                                                 causal, rows)
+            assert_close(to64(o2[0, h, rows]), o_ref, to64(l2[0, h, rows]), l_ref, what=f"pair N={N} head {h}")
+    finally:
+        del q, k, v
+        gc.collect()
+        torch.cuda.empty_cache()
