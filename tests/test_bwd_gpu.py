@@ -366,3 +366,41 @@ def test_backward_argument_errors(attn):
     assert call(ws_bytes=ws.numel() - 1) == attn.ATTN_ERR_WORKSPACE
     assert call(ws=None) == attn.ATTN_ERR_WORKSPACE
     assert call(d=96) == attn.ATTN_ERR_UNSUPPORTED
+
+
+# The backward's passes leave cleanly when a wait gives up: with a wait limit
+# of zero every role of the dK/dV and dQ kernels leaves its loop at the first
+# wait that is not already satisfied (copies drained, MMAs committed, TMEM
+# freed), attn_device_status reports ATTN_ERR_TIMEOUT, and the next call is
+# correct.  The CTAs that gave up still reset their scheduler slot, so 65 more
+# calls (every slot again) stay bit-identical.  Non-causal GQA with few units
+# runs the split dK/dV pass and its reduction.
+@pytest.mark.parametrize("d,causal", [(64, True), (128, True), (128, False)])
+def test_backward_timeout_is_reported_and_recovered(attn, d, causal):
+    dev = torch.device("cuda")
+    B, Hq, Hkv, N = 1, 8, 2, 700
+    q, k, v = prefill_inputs(92, B, Hq, Hkv, N, d, dev)
+    dout = output_grad(92, B, Hq, N, d, dev)
+    scale = scale_of(d)
+    o, lse = attn.forward(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == attn.ATTN_OK
+    old = attn.attn_set_wait_timeout_ns(0)
+    try:
+        attn.backward(q, k, v, o, lse, dout, causal=causal, scale=scale)
+        torch.cuda.synchronize()
+        assert attn.attn_device_status() == attn.ATTN_ERR_TIMEOUT
+    finally:
+        attn.attn_set_wait_timeout_ns(old)
+    assert attn.attn_device_status() == attn.ATTN_OK  # cleared by the read
+    grads = attn.backward(q, k, v, o, lse, dout, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == attn.ATTN_OK
+    refs = oracle.attention_bwd(to64(q), to64(k), to64(v), to64(dout), scale, causal)
+    for got, ref, name in zip(grads, refs, ("dq", "dk", "dv")):
+        assert_grad_close(to64(got), ref, f"{name} after timeout")
+    for i in range(65):
+        again = attn.backward(q, k, v, o, lse, dout, causal=causal, scale=scale)
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(again, grads)), f"call {i}"
+    assert attn.attn_device_status() == attn.ATTN_OK
