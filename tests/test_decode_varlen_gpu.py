@@ -161,3 +161,26 @@ def test_benchmark_workloads_every_element(attn, name, s_max, lens):
         del q, kc, vc
         gc.collect()
         torch.cuda.empty_cache()
+
+
+def test_timeout_is_reported_and_recovered(attn):
+    """With a wait limit of zero the work-list decode gives up at its first
+    unsatisfied wait (the planner and the merge have none), the status reads
+    ATTN_ERR_TIMEOUT, and the next call matches the oracle."""
+    dev = torch.device("cuda")
+    lens = [3000, 0, 17, 2500]
+    B, Hq, Hkv, d, s_max = len(lens), 16, 2, 128, 3000
+    q, kc, vc = decode_inputs(49, B, Hq, Hkv, s_max, d, dev)
+    seq = torch.tensor(lens, dtype=torch.int32, device=dev)
+    old = attn.attn_set_wait_timeout_ns(0)
+    try:
+        attn.decode_varlen(q, kc, vc, seq)
+        torch.cuda.synchronize()
+        assert attn.attn_device_status() == attn.ATTN_ERR_TIMEOUT
+    finally:
+        attn.attn_set_wait_timeout_ns(old)
+    o, _ = attn.decode_varlen(q, kc, vc, seq)
+    torch.cuda.synchronize()
+    assert attn.attn_device_status() == attn.ATTN_OK
+    o_ref, _ = oracle.decode(to64(q), to64(kc), to64(vc), lens, d ** -0.5)
+    assert_close(to64(o), o_ref, what="varlen after timeout")
