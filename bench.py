@@ -348,16 +348,22 @@ def run_gpu(args):
         e2e_step()
         torch.cuda.synchronize(dev)
         with ClockSampler(local) as e2e_clk:
+            # events between the calls (on the calls' own stream) give each
+            # call's device-side span without synchronising the host
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
             t0 = time.perf_counter()
-            for _ in range(reps):
+            marks[0].record(stream)
+            for i in range(reps):
                 e2e_step()
+                marks[i + 1].record(stream)
             torch.cuda.synchronize(dev)
             e2e_s = (time.perf_counter() - t0) / reps
+        per_call_ms = [round(marks[i].elapsed_time(marks[i + 1]), 3) for i in range(reps)]
         attn.check(attn.attn_device_status(sh), "e2e status")
         result["e2e"] = {"value": round(flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
                          "h2d_bytes_per_step": 3 * q.numel() * 2,
                          "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
-                         "steps": reps, "ms_per_step": round(e2e_s * 1e3, 3),
+                         "steps": reps, "ms_per_step": round(e2e_s * 1e3, 3), "per_call_ms": per_call_ms,
                          # the SM clock while these calls ran: the e2e loop comes after
                          # seconds of forward work, later than the step's own samples
                          "clocks": e2e_clk.summary(),
