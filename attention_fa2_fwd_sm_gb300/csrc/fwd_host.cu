@@ -175,8 +175,10 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
         ATTN_CK(cudaMemcpyAsync(slot + L.q_off, hq + q_at, q_bytes, cudaMemcpyHostToDevice, hp.in), "copy q");
         ATTN_CK(cudaMemcpyAsync(slot + L.k_off, hk + kv_at, kv_bytes, cudaMemcpyHostToDevice, hp.in), "copy k");
         ATTN_CK(cudaMemcpyAsync(slot + L.v_off, hv + kv_at, kv_bytes, cudaMemcpyHostToDevice, hp.in), "copy v");
-        ATTN_CK(cudaEventRecord(hp.in_done[s], hp.in), "cudaEventRecord (copy-in)");
+        // Each trace mark goes on its stream before the event other streams
+        // wait on, so a time on one stream never follows one that depends on it.
         ATTN_CK(trace_mark(c, 0, hp.in), "cudaEventRecord (trace)");
+        ATTN_CK(cudaEventRecord(hp.in_done[s], hp.in), "cudaEventRecord (copy-in)");
 
         cudaStream_t cs = (s == 0) ? stream : hp.comp;
         ATTN_CK(cudaStreamWaitEvent(cs, hp.in_done[s], 0), "wait (compute)");
@@ -196,8 +198,8 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
             join_internal();
             return rc;
         }
-        ATTN_CK(cudaEventRecord(hp.comp_done[s], cs), "cudaEventRecord (compute)");
         ATTN_CK(trace_mark(c, 2, cs), "cudaEventRecord (trace)");
+        ATTN_CK(cudaEventRecord(hp.comp_done[s], cs), "cudaEventRecord (compute)");
 
         ATTN_CK(cudaStreamWaitEvent(hp.out, hp.comp_done[s], 0), "wait (copy-out)");
         ATTN_CK(cudaMemcpyAsync(ho + q_at, slot + L.o_off, q_bytes, cudaMemcpyDeviceToHost, hp.out), "copy o");
@@ -205,8 +207,8 @@ int fwd_host_launch(const FwdHostLaunch &a, cudaStream_t stream) {
             ATTN_CK(cudaMemcpyAsync(a.lse_host + l_at, slot + L.lse_off, size_t(hn) * N * 4,
                                     cudaMemcpyDeviceToHost, hp.out),
                     "copy lse");
-        ATTN_CK(cudaEventRecord(hp.out_done[s], hp.out), "cudaEventRecord (copy-out)");
         ATTN_CK(trace_mark(c, 3, hp.out), "cudaEventRecord (trace)");
+        ATTN_CK(cudaEventRecord(hp.out_done[s], hp.out), "cudaEventRecord (copy-out)");
     }
     if (tracing) {
         tr.chunks = chunks;
